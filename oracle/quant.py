@@ -1,0 +1,118 @@
+"""Blockwise E4M3 quantisers (oracle side).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Source: "Puro-2B: Poor Lab's Qwen2-1.5B Trained on RTX 5090 within $5090"
+(papers.lianghsun.dev translation), section 3.2 "FP8 mixed-precision
+training": activations and activation gradients use 1-D groups of 128
+consecutive values along the GEMM reduction dimension, weights use 2-D
+128x128 blocks, and each group's scale is computed online from that group.
+The decoded value of a stored code is code * scale (the MXFP concept figure on
+the bloombook.cn tutorial page, "V_i = Q_i x X"), so the scale stored here is a
+dequantisation multiplier.
+
+One group G (128 values, or 128x128 values for a weight block) is quantised as
+
+1. amax = max |x| over G, in float32, ignoring NaN (fmaxf semantics);
+2. s = 1.0 if amax == 0 else float32(amax / 448)          (one IEEE division);
+3. q = E4M3_rn_satfinite(float32(x / s)) for every x in G (one IEEE division,
+   then one rounding to E4M3).
+
+Readings where the pages are silent: the scale is an arbitrary fp32 value
+amax/448 (not the power of two used on SM120); quantisation divides by s
+rather than multiplying by 448/amax; an all-zero group gets s = 1.
+
+Scale layouts (shared with the C ABI, which states the same contract):
+
+* quantize_act_1x128(X [R, C]) groups along C:  q [R, C],  s [C/128, R]
+  (s[g, r] is the scale of row r's g-th group: group-major, so the 128 row
+  scales of one group index are contiguous);
+* quantize_act_tokens_1x128(X [M, K]) groups along M (tokens) and stores the
+  transpose:  qT [K, M],  sT [M/128, K];
+* quantize_w_128x128(W [N, K]):  q [N, K],  qT [K, N] (= q transposed),
+  s [N/128, K/128].
+"""
+
+import numpy as np
+
+from .formats import e4m3_encode
+
+GROUP = 128
+E4M3_MAX = np.float32(448.0)
+
+
+def _check_bf16_grid(x, name):
+    x = np.asarray(x, dtype=np.float32)
+    if x.ndim != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if x.shape[0] % GROUP or x.shape[1] % GROUP:
+        raise ValueError(f"{name} dims must be multiples of {GROUP}, got {x.shape}")
+    return x
+
+
+def group_scale(amax):
+    """Scale of a group from its amax: amax/448 in fp32, or 1 when amax == 0."""
+    amax = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = amax / E4M3_MAX  # float32 / float32 -> float32, IEEE round to nearest
+    return np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+
+
+def quantize_values(x, s):
+    """q = E4M3(float32(x / s)), elementwise with broadcasting."""
+    x = np.asarray(x, dtype=np.float32)
+    s = np.asarray(s, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        y = x / s  # float32 division
+    return e4m3_encode(y)
+
+
+def quantize_act_1x128(x):
+    """Quantise X [R, C] in 1x128 groups along C.
+
+    Returns (q uint8 [R, C], s float32 [C/128, R]).
+    """
+    x = _check_bf16_grid(x, "x")
+    R, C = x.shape
+    xg = x.reshape(R, C // GROUP, GROUP)
+    amax = np.nanmax(np.abs(xg), axis=2) if xg.size else np.zeros((R, C // GROUP), np.float32)
+    s = group_scale(amax)  # [R, C/128]
+    q = quantize_values(xg, s[:, :, None]).reshape(R, C)
+    return q, np.ascontiguousarray(s.T)
+
+
+def quantize_act_tokens_1x128(x):
+    """Quantise X [M, K] in groups of 128 consecutive rows (tokens) per column.
+
+    This is the grouping that the weight-gradient GEMM needs, where the
+    reduction runs over tokens.  The codes are stored transposed.
+    Returns (qT uint8 [K, M], sT float32 [M/128, K]).
+    """
+    x = _check_bf16_grid(x, "x")
+    return quantize_act_1x128(np.ascontiguousarray(x.T))
+
+
+def quantize_w_128x128(w):
+    """Quantise W [N, K] in 128x128 blocks.
+
+    Returns (q uint8 [N, K], qT uint8 [K, N], s float32 [N/128, K/128]).
+    """
+    w = _check_bf16_grid(w, "w")
+    N, K = w.shape
+    wb = w.reshape(N // GROUP, GROUP, K // GROUP, GROUP)
+    amax = np.nanmax(np.abs(wb), axis=(1, 3)) if wb.size else np.zeros((N // GROUP, K // GROUP), np.float32)
+    s = group_scale(amax)  # [N/128, K/128]
+    q = quantize_values(wb, s[:, None, :, None]).reshape(N, K)
+    return q, np.ascontiguousarray(q.T), s
+
+
+def quantize_per_tensor(x):
+    """Comparator: one scale for the whole tensor (the scheme the paper moves
+    away from because a few outliers widen every value's quantisation step).
+
+    Returns (q uint8 same shape, s float32 scalar).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.nanmax(np.abs(x))) if x.size else np.float32(0)
+    s = group_scale(amax)
+    return quantize_values(x, s), np.float32(s)

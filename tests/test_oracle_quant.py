@@ -1,0 +1,174 @@
+"""Pins for the oracle's blockwise quantisers.
+
+Checked against: a hand-worked group (golden fixture), torch's float8 cast of
+a torch-computed x/s (library division and rounding), closed-form invariants
+of the amax/448 rule, the E4M3 round-trip error bound, group locality under
+single-element perturbations, and the paper's qualitative claim that local
+scales beat one scale per tensor when outliers are present.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden
+from oracle import formats, quant
+from blockwise_fp8_linear_quantise_b300 import workloads
+
+T_DEC = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def bf16_exact(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def test_worked_example_group():
+    rows = read_golden("quant_worked_example.txt")
+    assert rows[0][0] == "scale"
+    want_s = float(rows[0][1])
+    x = np.zeros((1, 128), np.float32)
+    want = np.zeros(128, np.uint8)
+    for pos, xv, _xs, code in rows[1:]:
+        x[0, int(pos)] = np.float32(float(xv))
+        want[int(pos)] = int(code, 16)
+    assert np.array_equal(bf16_exact(x).view(np.uint32), x.view(np.uint32))
+    q, s = quant.quantize_act_1x128(np.tile(x, (128, 1)))
+    assert s.shape == (1, 128) and np.all(s == want_s)
+    assert np.array_equal(q[0], want) and np.array_equal(q[77], want)
+
+
+def test_zero_group_gets_unit_scale():
+    x = np.zeros((128, 256), np.float32)
+    x[3, 130] = -0.0
+    x[5, 200] = 1.0
+    q, s = quant.quantize_act_1x128(x)
+    assert s[0, 3] == 1.0 and s[1, 3] == 1.0 and s[0, 5] == 1.0
+    assert q[3, 130] == 0x80 and np.count_nonzero(q[3]) == 1
+    assert s[1, 5] == np.float32(1.0) / np.float32(448.0) and q[5, 200] == 0x7E
+
+
+def test_quantised_codes_match_torch_cast_of_library_division():
+    wl = workloads.make("tiny")
+    x = workloads.tensor(wl, "x").float().numpy()
+    q, s = quant.quantize_act_1x128(x)
+    # independent: group amax and division via torch, cast via torch float8
+    xt = torch.from_numpy(x).view(256, 2, 128)
+    amax = xt.abs().amax(dim=2)
+    st = amax / 448.0
+    assert np.array_equal(st.numpy(), s.T)
+    y = xt / st[:, :, None]
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(256, 256).numpy()
+    assert np.array_equal(q, ref)
+
+
+def test_every_bf16_pattern_in_groups():
+    # all finite bf16 values, arranged in groups of 128 with a shared anchor
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = bits[np.isfinite(bits)]
+    n = vals.size - vals.size % 127
+    g = vals[:n].reshape(-1, 127)
+    for anchor in (1.0, 3.0e38, 2.0 ** -100):
+        x = np.concatenate([np.full((g.shape[0], 1), anchor, np.float32), g], axis=1)
+        x = x[: (x.shape[0] // 128) * 128]
+        q, s = quant.quantize_act_1x128(x)
+        amax = np.abs(x).max(axis=1)
+        st = torch.from_numpy(amax) / 448.0
+        assert np.array_equal(s[0], st.numpy())
+        ref = (torch.from_numpy(x) / st[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        ok = np.isfinite(x / s[0][:, None]) & (np.abs(x / s[0][:, None]) <= 448)
+        assert np.array_equal(q[ok], ref[ok])
+        assert np.all(np.abs(T_DEC[q]) <= 448)
+
+
+def _roundtrip_ok(x, q, s_full):
+    dq = T_DEC[q] * s_full.astype(np.float64)
+    err = np.abs(x.astype(np.float64) - dq)
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s_full) * (1 + 2.0 ** -20) + 1e-45
+    return np.all(err <= bound)
+
+
+@pytest.mark.parametrize("name,tag", [("tiny", "x"), ("tiny", "w")])
+def test_invariants_rows_tokens_weights(name, tag):
+    wl = workloads.make(name)
+    x = workloads.tensor(wl, tag).float().numpy()
+    R, C = x.shape
+    # rows
+    q, s = quant.quantize_act_1x128(x)
+    assert q.shape == (R, C) and s.shape == (C // 128, R)
+    s_full = np.repeat(s.T, 128, axis=1)
+    assert _roundtrip_ok(x, q, s_full)
+    assert np.all(np.abs(T_DEC[q]) <= 448)
+    for r in range(R):
+        for g in range(C // 128):
+            grp = q[r, g * 128:(g + 1) * 128]
+            assert np.any((grp == 0x7E) | (grp == 0xFE))
+            amax = np.abs(x[r, g * 128:(g + 1) * 128]).max()
+            assert abs(float(s[g, r]) * 448.0 - amax) <= amax * 2.0 ** -23
+    # tokens (transposed storage)
+    qT, sT = quant.quantize_act_tokens_1x128(x)
+    assert qT.shape == (C, R) and sT.shape == (R // 128, C)
+    sT_full = np.repeat(sT, 128, axis=0)  # [R, C] scale of x[r, c]
+    assert _roundtrip_ok(x, qT.T, sT_full)
+    # weights
+    wq, wqT, ws = quant.quantize_w_128x128(x)
+    assert wq.shape == (R, C) and np.array_equal(wqT, wq.T) and ws.shape == (R // 128, C // 128)
+    ws_full = np.repeat(np.repeat(ws, 128, axis=0), 128, axis=1)
+    assert _roundtrip_ok(x, wq, ws_full)
+    for b in range(R // 128):
+        for c in range(C // 128):
+            blk = wq[b * 128:(b + 1) * 128, c * 128:(c + 1) * 128]
+            assert np.any((blk == 0x7E) | (blk == 0xFE))
+
+
+def test_power_of_two_amax_gives_exact_scale():
+    x = np.zeros((128, 128), np.float32)
+    for r in range(128):
+        x[r, r] = np.float32(448.0 * 2.0 ** (r - 64))
+    _, s = quant.quantize_act_1x128(x)
+    assert np.array_equal(s[0], np.float32(2.0) ** (np.arange(128) - 64).astype(np.float32))
+
+
+def test_group_locality():
+    rng = np.random.default_rng(3)
+    x = bf16_exact(rng.standard_normal((256, 384)))
+    q, s = quant.quantize_act_1x128(x)
+    qT, sT = quant.quantize_act_tokens_1x128(x)
+    wq, _, ws = quant.quantize_w_128x128(x)
+    r0, c0 = 200, 260
+    y = x.copy()
+    y[r0, c0] = 100.0
+    q2, s2 = quant.quantize_act_1x128(y)
+    qT2, sT2 = quant.quantize_act_tokens_1x128(y)
+    wq2, _, ws2 = quant.quantize_w_128x128(y)
+    # rows: only group (r0, c0//128) changes
+    ds = np.argwhere(s != s2)
+    assert ds.tolist() == [[c0 // 128, r0]]
+    dq = np.argwhere(q != q2)
+    assert np.all(dq[:, 0] == r0) and np.all(dq[:, 1] // 128 == c0 // 128)
+    # tokens: only group (r0//128, c0) changes
+    assert np.argwhere(sT != sT2).tolist() == [[r0 // 128, c0]]
+    dqT = np.argwhere(qT != qT2)
+    assert np.all(dqT[:, 0] == c0) and np.all(dqT[:, 1] // 128 == r0 // 128)
+    # weight block: only block (r0//128, c0//128) changes
+    assert np.argwhere(ws != ws2).tolist() == [[r0 // 128, c0 // 128]]
+    dw = np.argwhere(wq != wq2)
+    assert np.all(dw[:, 0] // 128 == r0 // 128) and np.all(dw[:, 1] // 128 == c0 // 128)
+
+
+def _rel_fro(x, dq):
+    return np.linalg.norm(x - dq) / np.linalg.norm(x)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mlp_gateup"])
+def test_blockwise_beats_per_tensor_on_outliers(name):
+    wl = workloads.make(name)
+    x = workloads.tensor(wl, "x").float().numpy()
+    if x.shape[0] > 2048:
+        x = x[:2048]
+    x = x.astype(np.float64)
+    q, s = quant.quantize_act_1x128(x)
+    blk = _rel_fro(x, T_DEC[q] * np.repeat(s.T, 128, axis=1))
+    qt, st = quant.quantize_per_tensor(x)
+    per = _rel_fro(x, T_DEC[qt] * float(st))
+    assert blk < per
+    assert blk < 0.05
