@@ -1,0 +1,456 @@
+// C ABI of the blockwise-FP8 linear layer: argument validation, tensor-map
+// encoding, launch configuration and the fused linear forward/backward.
+// All kernels live in this single translation unit (quant.cuh, gemm.cuh) so
+// the device error word has one definition per loaded module.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bfp8.h"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace {
+
+using namespace bfp8;
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  uint64_t wait_ns = kDefaultWaitNs;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_forced_splits = 0;  // 0 = automatic
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bfp8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BFP8_OK : BFP8_ECUDA; }
+
+// Looks up the current device, checks it is an sm_103 part and sets the
+// kernels' shared-memory limits once.
+bfp8_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BFP8_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BFP8_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BFP8_ECUDA;
+    if (major != 10 || minor != 3) return BFP8_EUNSUPPORTED;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return BFP8_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cudaError_t e = cudaSuccess;
+    e = cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+#define BFP8_SET_GEMM_SMEM(BN, MODE)                                                                     \
+  if (e == cudaSuccess)                                                                                   \
+    e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             GemmSmem<BN>::kAlloc);
+    BFP8_SET_GEMM_SMEM(256, kSbBlock)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT)
+    BFP8_SET_GEMM_SMEM(256, kSbCol)
+    BFP8_SET_GEMM_SMEM(128, kSbBlock)
+    BFP8_SET_GEMM_SMEM(128, kSbBlockT)
+    BFP8_SET_GEMM_SMEM(128, kSbCol)
+#undef BFP8_SET_GEMM_SMEM
+    if (e != cudaSuccess) return BFP8_ECUDA;
+    // The GEMM moves registers between warpgroups with setmaxnreg; that is
+    // only safe if each thread really starts with kLaunchRegs registers.
+    // Refuse to run a build where it does not (it would wait forever).
+#define BFP8_CHECK_REGS(BN, MODE)                                                  \
+  {                                                                                 \
+    cudaFuncAttributes fa;                                                          \
+    if (cudaFuncGetAttributes(&fa, block_gemm_kernel<BN, MODE>) != cudaSuccess) \
+      return BFP8_ECUDA;                                                            \
+    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                        \
+  }
+    BFP8_CHECK_REGS(256, kSbBlock)
+    BFP8_CHECK_REGS(256, kSbBlockT)
+    BFP8_CHECK_REGS(256, kSbCol)
+    BFP8_CHECK_REGS(128, kSbBlock)
+    BFP8_CHECK_REGS(128, kSbBlockT)
+    BFP8_CHECK_REGS(128, kSbCol)
+#undef BFP8_CHECK_REGS
+    st.sms = sms;
+    st.ready = true;
+  }
+  *out = &st;
+  return BFP8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int64_t d) { return d > 0 && d % 128 == 0 && d <= (int64_t(1) << 30); }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 2-D K-contiguous E4M3 tensor [rows, K], box 128 (K bytes) x box_rows,
+// 128-byte swizzle: the shared-memory image is the canonical K-major
+// layout the MMA descriptors describe.
+bfp8_status make_kmajor_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
+}
+
+struct GemmPlan {
+  int bn;
+  int m_tiles, n_tiles, tiles;
+  int splits, kps;
+  size_t ws_bytes;
+};
+
+// Picks the column tile and the split-K factor.  Split-K only pays when the
+// tile count leaves SMs idle and the extra fp32 partial traffic is small next
+// to the GEMM time; estimate both with nominal B300 rates.
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms) {
+  GemmPlan g;
+  g.bn = (N % 256 == 0) ? 256 : 128;
+  g.m_tiles = static_cast<int>(M / 128);
+  g.n_tiles = static_cast<int>(N / g.bn);
+  g.tiles = g.m_tiles * g.n_tiles;
+  const int nk = static_cast<int>(K / 128);
+  int best = 1;
+  if (g_forced_splits > 0) {
+    best = std::min(g_forced_splits, nk);
+  } else if (sms > 0) {
+    const double t_gemm = 2.0 * M * N * K / 4.0e15;
+    double best_t = 1e30;
+    for (int s = 1; s <= std::min(nk, 16); ++s) {
+      const int units = g.tiles * s;
+      const double waves = std::ceil(static_cast<double>(units) / sms);
+      const double eff = units / (waves * sms);
+      const double t = t_gemm / eff + (s > 1 ? (static_cast<double>(s) * M * N * 4 * 2 + M * N * 2) / 6.0e12 : 0.0);
+      if (t < best_t * 0.97) {
+        best_t = t;
+        best = s;
+      }
+    }
+  }
+  g.kps = (nk + best - 1) / best;
+  g.splits = (nk + g.kps - 1) / g.kps;
+  g.ws_bytes = g.splits > 1 ? static_cast<size_t>(g.splits) * M * N * sizeof(float) : 0;
+  return g;
+}
+
+template <int BN>
+bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+                           cudaStream_t st) {
+  const int smem = GemmSmem<BN>::kAlloc;
+  switch (mode) {
+    case kSbBlock:
+      block_gemm_kernel<BN, kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      break;
+    case kSbBlockT:
+      block_gemm_kernel<BN, kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      break;
+    default:
+      block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      break;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+bfp8_status launch_quant(const QuantParams& p, bool weight, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(p.C / 128), static_cast<unsigned>(p.R / 128));
+  if (p.R / 128 > 65535) return BFP8_EUNSUPPORTED;
+  if (weight)
+    quantize_tile_kernel<true><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
+  else
+    quantize_tile_kernel<false><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
+  return cuda_status(cudaGetLastError());
+}
+
+bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                      int64_t M, int64_t N, int64_t K, void* C, uint8_t* Cq, float* sCq, void* ws, size_t ws_bytes,
+                      cudaStream_t stream) {
+  if (layout != BFP8_FPROP && layout != BFP8_DGRAD && layout != BFP8_WGRAD) return BFP8_EINVAL;
+  if (!A || !sa || !B || !sb || !C) return BFP8_EINVAL;
+  if ((Cq == nullptr) != (sCq == nullptr)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sa) || !aligned16(sb) || !aligned16(C) ||
+      (Cq && (!aligned16(Cq) || !aligned16(sCq))))
+    return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  const GemmPlan g = plan_gemm(M, N, K, dev->sms);
+  if (g.ws_bytes > 0) {
+    if (ws == nullptr || ws_bytes < g.ws_bytes) return BFP8_EWORKSPACE;
+    if (!aligned16(ws)) return BFP8_EALIGN;
+  }
+  CUtensorMap ta, tb;
+  if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
+  if ((s = make_kmajor_tmap(&tb, B, N, K, g.bn)) != BFP8_OK) return s;
+
+  GemmParams p;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_tiles = g.m_tiles;
+  p.n_tiles = g.n_tiles;
+  p.tiles = g.tiles;
+  p.splits = g.splits;
+  p.kps = g.kps;
+  p.units = g.tiles * g.splits;
+  p.group_m = 16;
+  p.sa = sa;
+  p.sb = sb;
+  p.C = static_cast<uint16_t*>(C);
+  p.Cpart = g.splits > 1 ? static_cast<float*>(ws) : nullptr;
+  // The fused quantised epilogue needs a whole 128-column group per thread,
+  // which the 256-column tile gives; otherwise the codes come from the
+  // split-K reduction or from the row quantiser run on C afterwards.
+  const bool fused_here = g.splits == 1 && g.bn == 256;
+  p.Cq = fused_here ? Cq : nullptr;
+  p.sCq = fused_here ? sCq : nullptr;
+  p.wait_ns = dev->wait_ns;
+  const int mode = layout == BFP8_FPROP ? kSbBlock : (layout == BFP8_DGRAD ? kSbBlockT : kSbCol);
+  const int grid = std::min(p.units, dev->sms);
+  s = g.bn == 256 ? launch_gemm_bn<256>(mode, ta, tb, p, grid, stream)
+                  : launch_gemm_bn<128>(mode, ta, tb, p, grid, stream);
+  if (s != BFP8_OK) return s;
+  if (g.splits == 1) {
+    if (Cq == nullptr || fused_here) return BFP8_OK;
+    QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns};
+    return launch_quant(qp, false, stream);
+  }
+  const int64_t groups = M * (N / 128);
+  const int rgrid = static_cast<int>(std::min<int64_t>((groups + 7) / 8, int64_t(dev->sms) * 16));
+  splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(static_cast<const float*>(ws), g.splits, p.M, p.N,
+                                                   static_cast<uint16_t*>(C), Cq, sCq);
+  return cuda_status(cudaGetLastError());
+}
+
+bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                           cudaStream_t stream) {
+  if (!x || (!q && !qT)) return BFP8_EINVAL;
+  if ((q && !s) || (qT && !sT)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(K)) return BFP8_EINVAL;
+  if (!aligned16(x) || (q && (!aligned16(q) || !aligned16(s))) || (qT && (!aligned16(qT) || !aligned16(sT))))
+    return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status st = device_state(&dev);
+  if (st != BFP8_OK) return st;
+  QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns};
+  return launch_quant(p, false, stream);
+}
+
+bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s, cudaStream_t stream) {
+  if (!w || !s || (!q && !qT)) return BFP8_EINVAL;
+  if (!dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  if (!aligned16(w) || !aligned16(s) || (q && !aligned16(q)) || (qT && !aligned16(qT))) return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status st = device_state(&dev);
+  if (st != BFP8_OK) return st;
+  QuantParams p{static_cast<const uint16_t*>(w), N, K, q, s, qT, nullptr, dev->wait_ns};
+  return launch_quant(p, true, stream);
+}
+
+// Workspace carving for the fused linear calls: consecutive 256-byte aligned
+// regions.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off = round_up(off + bytes, 256);
+    return p;
+  }
+};
+
+size_t fwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** Wq, uint8_t** Xq, float** sX,
+              void** gws) {
+  Carver local(nullptr);
+  Carver& cv = c ? *c : local;
+  uint8_t* wq = cv.take<uint8_t>(static_cast<size_t>(N) * K);
+  uint8_t* xq = cv.take<uint8_t>(static_cast<size_t>(M) * K);
+  float* sx = cv.take<float>(static_cast<size_t>(K / 128) * M * sizeof(float));
+  const GemmPlan g = plan_gemm(M, N, K, sms);
+  void* gw = cv.take<uint8_t>(g.ws_bytes);
+  if (Wq) *Wq = wq;
+  if (Xq) *Xq = xq;
+  if (sX) *sX = sx;
+  if (gws) *gws = gw;
+  return cv.off;
+}
+
+size_t bwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** dYq, float** sdY, uint8_t** dYqT,
+              float** sdYT, void** gws) {
+  Carver local(nullptr);
+  Carver& cv = c ? *c : local;
+  uint8_t* a = cv.take<uint8_t>(static_cast<size_t>(M) * N);
+  float* b = cv.take<float>(static_cast<size_t>(N / 128) * M * sizeof(float));
+  uint8_t* cT = cv.take<uint8_t>(static_cast<size_t>(N) * M);
+  float* d = cv.take<float>(static_cast<size_t>(M / 128) * N * sizeof(float));
+  const GemmPlan gd = plan_gemm(M, K, N, sms);   // dgrad: [M, K], reduction N
+  const GemmPlan gw = plan_gemm(N, K, M, sms);   // wgrad: [N, K], reduction M
+  void* w = cv.take<uint8_t>(std::max(gd.ws_bytes, gw.ws_bytes));
+  if (dYq) *dYq = a;
+  if (sdY) *sdY = b;
+  if (dYqT) *dYqT = cT;
+  if (sdYT) *sdYT = d;
+  if (gws) *gws = w;
+  return cv.off;
+}
+
+int current_sms() {
+  DeviceState* dev = nullptr;
+  return device_state(&dev) == BFP8_OK ? dev->sms : 148;
+}
+
+}  // namespace
+
+extern "C" {
+
+bfp8_status bfp8_quantize_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                    bfp8_stream_t stream) {
+  return quant_act_impl(x, M, K, q, s, qT, sT, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_quantize_w_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s,
+                                    bfp8_stream_t stream) {
+  return quant_w_impl(w, N, K, q, qT, s, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B,
+                                const float* sb, int64_t M, int64_t N, int64_t K, void* C, uint8_t* Cq, float* sCq,
+                                void* workspace, size_t ws_bytes, bfp8_stream_t stream) {
+  return gemm_impl(layout, A, sa, B, sb, M, N, K, C, Cq, sCq, workspace, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K) {
+  (void)layout;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
+  return plan_gemm(M, N, K, current_sms()).ws_bytes;
+}
+
+size_t bfp8_linear_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
+  return fwd_ws(M, N, K, current_sms(), nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
+  return bwd_ws(M, N, K, current_sms(), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
+                            float* sW, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+  if (!X || !W || !Y || !WqT || !sW || !XqT || !sXT) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  const size_t need = fwd_ws(M, N, K, dev->sms, nullptr, nullptr, nullptr, nullptr, nullptr);
+  if (ws == nullptr || ws_bytes < need) return BFP8_EWORKSPACE;
+  if (!aligned16(ws)) return BFP8_EALIGN;
+  Carver cv(ws);
+  uint8_t *Wq, *Xq;
+  float* sX;
+  void* gws;
+  fwd_ws(M, N, K, dev->sms, &cv, &Wq, &Xq, &sX, &gws);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = quant_w_impl(W, N, K, Wq, WqT, sW, st)) != BFP8_OK) return s;
+  if ((s = quant_act_impl(X, M, K, Xq, sX, XqT, sXT, st)) != BFP8_OK) return s;
+  const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
+  return gemm_impl(BFP8_FPROP, Xq, sX, Wq, sW, M, N, K, Y, nullptr, nullptr, gws, gws_bytes, st);
+}
+
+bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT, const float* sXT,
+                            int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws, size_t ws_bytes,
+                            bfp8_stream_t stream) {
+  if (!dY || !WqT || !sW || !XqT || !sXT || !dX || !dW) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  const size_t need = bwd_ws(M, N, K, dev->sms, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  if (ws == nullptr || ws_bytes < need) return BFP8_EWORKSPACE;
+  if (!aligned16(ws)) return BFP8_EALIGN;
+  Carver cv(ws);
+  uint8_t *dYq, *dYqT;
+  float *sdY, *sdYT;
+  void* gws;
+  bwd_ws(M, N, K, dev->sms, &cv, &dYq, &sdY, &dYqT, &sdYT, &gws);
+  const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = quant_act_impl(dY, M, N, dYq, sdY, dYqT, sdYT, st)) != BFP8_OK) return s;
+  if ((s = gemm_impl(BFP8_DGRAD, dYq, sdY, WqT, sW, M, K, N, dX, nullptr, nullptr, gws, gws_bytes, st)) != BFP8_OK)
+    return s;
+  return gemm_impl(BFP8_WGRAD, dYqT, sdYT, XqT, sXT, N, K, M, dW, nullptr, nullptr, gws, gws_bytes, st);
+}
+
+bfp8_status bfp8_sync_status(bfp8_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BFP8_ECUDA;
+  unsigned int flags = 0;
+  if (cudaMemcpyFromSymbol(&flags, bfp8::g_error_flags, sizeof(flags)) != cudaSuccess) return BFP8_ECUDA;
+  if (flags != 0u) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(bfp8::g_error_flags, &zero, sizeof(zero)) != cudaSuccess) return BFP8_ECUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return BFP8_ECUDA;
+  }
+  return (flags & bfp8::kErrTimeout) ? BFP8_ETIMEOUT : BFP8_OK;
+}
+
+bfp8_status bfp8_set_wait_limit_ns(uint64_t ns) {
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  dev->wait_ns = ns == 0 ? kDefaultWaitNs : ns;
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_set_gemm_splits(int splits) {
+  if (splits < 0) return BFP8_EINVAL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_forced_splits = splits;
+  return BFP8_OK;
+}
+
+const char* bfp8_status_string(bfp8_status status) {
+  switch (status) {
+    case BFP8_OK: return "ok";
+    case BFP8_EINVAL: return "invalid argument (null pointer, bad enum, or a dimension not a positive multiple of 128)";
+    case BFP8_EALIGN: return "pointer not 16-byte aligned";
+    case BFP8_EUNSUPPORTED: return "unsupported device or size";
+    case BFP8_ECUDA: return "CUDA runtime or driver error";
+    case BFP8_ETIMEOUT: return "device-side bounded wait expired";
+    case BFP8_EWORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

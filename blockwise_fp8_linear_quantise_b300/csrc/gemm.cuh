@@ -1,0 +1,443 @@
+// Block-scaled E4M3 GEMM with fp32 promotion of every 128-deep slice.
+//
+// Computes C[i, j] = bf16( sum_kb P_kb[i, j] * sa(i, kb) * sb(j, kb) ) with
+// P_kb the E4M3 x E4M3 product over the 128 reduction indices of slice kb,
+// the GEMM of the Transformer linear layers in "Puro-2B: Poor Lab's
+// Qwen2-1.5B Trained on RTX 5090 within $5090", section 3.2 (E4M3 operands,
+// one scale per 1x128 activation group and per 128x128 weight block).
+//
+// The per-group scales are arbitrary fp32 values, which the tensor cores'
+// own block-scale path (power-of-two or E4M3 scale factors per 16/32
+// elements) cannot express, so every slice's partial product leaves the
+// tensor core and is promoted in fp32 by CUDA cores:
+//
+//   warp 8      TMA producer: per slice, a 128x128 A tile and a BNx128 B tile
+//               (both 128-byte swizzled) into a STAGES-deep shared-memory ring.
+//   warp 9      MMA issuer: 4 x tcgen05.mma (K=32 each) write the slice's
+//               partial P_kb into one of two TMEM buffers (BN fp32 columns
+//               each); commits release the smem stage and signal the buffer.
+//   warps 0..7  promotion: warp w reads TMEM lanes 32*(w%4).. (its 32 rows)
+//               and columns 128*(w/4).. of the buffer, multiplies by the
+//               slice's scale product and adds into 128 fp32 accumulators
+//               per thread held in registers, then frees the buffer.  While
+//               they promote slice kb the tensor core already computes kb+1.
+//               At the end of a tile they convert to bf16 (optionally also
+//               E4M3 codes of the bf16 output) and store.
+//
+// The kernel is persistent: one CTA per SM walks work units (tile, split)
+// in a grouped order that keeps a band of A rows and B rows hot in L2.
+// With split-K, each split writes fp32 partial sums to a workspace and a
+// separate kernel adds them in a fixed order (deterministic).
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace bfp8 {
+
+enum SbMode : int {
+  kSbBlock = 0,   // sb [N/128, K/128]: FPROP weight blocks
+  kSbBlockT = 1,  // sb [K/128, N/128]: DGRAD weight blocks (transposed use)
+  kSbCol = 2      // sb [K/128, N]:     WGRAD per-column token groups
+};
+
+struct GemmParams {
+  int M, N, K;
+  int m_tiles, n_tiles, tiles;  // tiles = m_tiles * n_tiles
+  int splits, kps;              // split-K count and slices per split
+  int units;                    // tiles * splits
+  int group_m;                  // tile rasterisation band height (in m tiles)
+  const float* sa;              // [K/128, M]
+  const float* sb;              // see SbMode
+  uint16_t* C;                  // bf16 [M, N] (splits == 1)
+  float* Cpart;                 // fp32 [splits, M, N] (splits > 1)
+  uint8_t* Cq;                  // optional E4M3 [M, N] (splits == 1)
+  float* sCq;                   // optional [N/128, M]
+  uint64_t wait_ns;
+};
+
+// Three warpgroups: 0 and 1 promote, 2 holds the producer (warp 8) and the
+// MMA issuer (warp 9); warps 10 and 11 only give their registers away.
+// At launch every thread has kLaunchRegs registers (65536 / 384, rounded
+// down to a multiple of 8); warpgroup 2 then drops to kSmallRegs and the
+// promotion warpgroups rise to kBigRegs.  The split adds up exactly:
+// 128 * 56 + 256 * 224 = 384 * 168.
+constexpr int kGemmThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kLaunchRegs = 168;
+constexpr int kSmallRegs = 56;
+constexpr int kBigRegs = 224;
+static_assert(128 * kSmallRegs + 256 * kBigRegs <= kGemmThreads * kLaunchRegs, "register split exceeds the launch");
+constexpr int kStages = 4;
+
+template <int BN>
+struct GemmSmem {
+  static constexpr int kABytes = 128 * 128;
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kAOff = 0;
+  static constexpr int kBOff = kStages * kABytes;
+  static constexpr int kRingOff = kBOff + kStages * kBBytes;  // float[2][BN] per-column scales
+  static constexpr int kBarOff = kRingOff + 2 * BN * 4;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], done, ring[2]
+  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kTmemSlotOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+  static constexpr uint32_t kTmemCols = 2 * BN;
+};
+
+struct UnitCoords {
+  int m0;     // first output row
+  int nt;     // output column tile index (columns nt*BN ..)
+  int split;  // split-K index
+  int kb0, kb1;  // slice range [kb0, kb1)
+};
+
+__device__ __forceinline__ UnitCoords unit_coords(const GemmParams& p, int u) {
+  UnitCoords c;
+  const int tile = u % p.tiles;
+  c.split = u / p.tiles;
+  const int per_group = p.group_m * p.n_tiles;
+  const int g = tile / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.m_tiles - first_m, p.group_m);
+  const int in_g = tile - g * per_group;
+  c.m0 = (first_m + in_g % gm) * 128;
+  c.nt = in_g / gm;
+  const int nk = p.K / 128;
+  c.kb0 = c.split * p.kps;
+  c.kb1 = min(nk, c.kb0 + p.kps);
+  return c;
+}
+
+template <int BN, int SBMODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const GemmParams p) {
+  using L = GemmSmem<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint64_t* done = bars + 2 * kStages + 4;
+  uint64_t* ringbar = bars + 2 * kStages + 5;  // per-column scale slots filled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
+  float* ring = reinterpret_cast<float*>(smem + L::kRingOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 8);  // one arrival per promotion warp
+    }
+    mbar_init(done, 1);
+    mbar_init(&ringbar[0], 256);
+    mbar_init(&ringbar[1], 256);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp >= kProducerWarp) {
+    setmaxnreg_dec<kSmallRegs>();
+    if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const UnitCoords c = unit_coords(p, u);
+        for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, 0x301u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], L::kABytes + L::kBBytes);
+          tma_load_2d(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, c.m0, &full[s]);
+          tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128, c.nt * BN, &full[s]);
+        }
+      }
+      // Do not leave while copies into this CTA's shared memory are in flight:
+      // wait for the last fill of every stage to land.
+      for (uint32_t j = 0; j < kStages && j < it; ++j) {
+        const uint32_t f = it - 1 - j;
+        mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
+      }
+    }
+    } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const UnitCoords c = unit_coords(p, u);
+        for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+          if (!mbar_wait(&tempty[b], bph ^ 1u, p.wait_ns, 0x311u) || !mbar_wait(&full[s], ph, p.wait_ns, 0x312u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes);
+          const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes);
+          const uint32_t d = tmem_base + b * BN;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_e4m3(d, sw128_kmajor_desc(a_addr + 32 * k), sw128_kmajor_desc(b_addr + 32 * k), idesc, k > 0);
+          mma_commit(&empty[s]);
+          mma_commit(&tfull[b]);
+        }
+      }
+      // Every MMA this thread issued has completed once `done` fires.
+      mma_commit(done);
+      mbar_wait(done, 0, p.wait_ns, 0x313u);
+    }
+    }
+  } else {
+    setmaxnreg_inc<kBigRegs>();
+    // ------------------------------------------------------------ promotion
+    constexpr int kCols = BN / 2;  // output columns per promotion thread
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int nkb = p.K / 128;
+    uint32_t it = 0;
+    bool ok = true;
+    float acc[kCols];
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const UnitCoords c = unit_coords(p, u);
+      const int gm = c.m0 + row;
+      const int col0 = c.nt * BN + half * kCols;  // first output column of this thread
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
+
+      // Scale pointers for this unit, advanced one slice at a time:
+      //   sa      [K/128, M]  -> this thread's row, stride M per slice
+      //   sb mode kSbBlock  [N/128, K/128] -> this thread's column block, stride 1
+      //   sb mode kSbBlockT [K/128, N/128] -> stride N/128
+      //   sb mode kSbCol    [K/128, N]     -> thread t's column (ring fill), stride N
+      const float* sa_ptr = p.sa + static_cast<int64_t>(c.kb0) * p.M + gm;
+      const float* sb_ptr;
+      int64_t sb_stride;
+      if constexpr (SBMODE == kSbBlock) {
+        sb_ptr = p.sb + static_cast<int64_t>(col0 / 128) * nkb + c.kb0;
+        sb_stride = 1;
+      } else if constexpr (SBMODE == kSbBlockT) {
+        sb_ptr = p.sb + static_cast<int64_t>(c.kb0) * (p.N / 128) + col0 / 128;
+        sb_stride = p.N / 128;
+      } else {
+        sb_ptr = p.sb + static_cast<int64_t>(c.kb0) * p.N + c.nt * BN + threadIdx.x;
+        sb_stride = p.N;
+      }
+      const bool col_loader = (BN == 256) || (threadIdx.x < BN);
+      float sa_next = __ldg(sa_ptr);
+      float sb_next = 0.0f;
+      if constexpr (SBMODE != kSbCol) {
+        sb_next = __ldg(sb_ptr);
+      } else {
+        // Slot it&1 holds the column scales of slice `it`; every promotion
+        // thread writes (at most) one value and arrives, readers wait for all 256.
+        if (col_loader) ring[(it & 1u) * BN + threadIdx.x] = __ldg(sb_ptr);
+        mbar_arrive(&ringbar[it & 1u]);
+      }
+
+      for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+        const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+        const float sa_cur = sa_next;
+        const float sb_cur = sb_next;
+        float col_next = 0.0f;
+        if (kb + 1 < c.kb1) {
+          sa_ptr += p.M;
+          sb_ptr += sb_stride;
+          sa_next = __ldg(sa_ptr);
+          if constexpr (SBMODE != kSbCol) {
+            sb_next = __ldg(sb_ptr);
+          } else {
+            if (col_loader) col_next = __ldg(sb_ptr);
+          }
+        }
+        if constexpr (SBMODE == kSbCol) {
+          if (!mbar_wait(&ringbar[b], bph, p.wait_ns, 0x322u)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!mbar_wait(&tfull[b], bph, p.wait_ns, 0x321u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_base + b * BN + half * kCols;
+        if constexpr (SBMODE != kSbCol) {
+          const float s = sa_cur * sb_cur;
+          const float2 s2 = make_float2(s, s);
+#pragma unroll
+          for (int r = 0; r < kCols / 64; ++r) {
+            uint32_t v[64];
+            tmem_ld32(taddr + r * 64, v);
+            tmem_ld32(taddr + r * 64 + 32, v + 32);
+            tmem_wait_ld64(v);
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+              float2 a2 = make_float2(acc[r * 64 + i], acc[r * 64 + i + 1]);
+              a2 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), s2, a2);
+              acc[r * 64 + i] = a2.x;
+              acc[r * 64 + i + 1] = a2.y;
+            }
+            reg_fence64(acc + r * 64);
+          }
+        } else {
+          const float* sbc = ring + b * BN + half * kCols;
+          const float2 sa2 = make_float2(sa_cur, sa_cur);
+#pragma unroll
+          for (int r = 0; r < kCols / 64; ++r) {
+            uint32_t v[64];
+            tmem_ld32(taddr + r * 64, v);
+            tmem_ld32(taddr + r * 64 + 32, v + 32);
+            tmem_wait_ld64(v);
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              const float4 sb4 = *reinterpret_cast<const float4*>(sbc + r * 64 + i);
+              const float2 sc0 = fmul2(sa2, make_float2(sb4.x, sb4.y));
+              const float2 sc1 = fmul2(sa2, make_float2(sb4.z, sb4.w));
+              float2 a0 = make_float2(acc[r * 64 + i], acc[r * 64 + i + 1]);
+              float2 a1 = make_float2(acc[r * 64 + i + 2], acc[r * 64 + i + 3]);
+              a0 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc0, a0);
+              a1 = ffma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), sc1, a1);
+              acc[r * 64 + i] = a0.x;
+              acc[r * 64 + i + 1] = a0.y;
+              acc[r * 64 + i + 2] = a1.x;
+              acc[r * 64 + i + 3] = a1.y;
+            }
+            reg_fence64(acc + r * 64);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        if constexpr (SBMODE == kSbCol) {
+          // Everyone has passed this slice's ring wait, so every thread is
+          // done with slot (it+1)&1 (last read for slice it-1): refill it.
+          if (kb + 1 < c.kb1) {
+            if (col_loader) ring[((it + 1) & 1u) * BN + threadIdx.x] = col_next;
+            mbar_arrive(&ringbar[(it + 1) & 1u]);
+          }
+        }
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ epilogue
+      if (p.splits == 1) {
+        // bf16 output, 8 columns (16 bytes) per store.
+        uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.N + col0;
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kCols / 8; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+          }
+          *reinterpret_cast<uint4*>(crow + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if constexpr (BN == 256) {
+          if (p.Cq != nullptr) {
+          // E4M3 codes of the bf16 values of this thread's 128-column group,
+          // with the activation quantiser's rule (m is their amax).
+          const float s = group_scale(m);
+          uint8_t* qrow = p.Cq + static_cast<int64_t>(gm) * p.N + col0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = 16 * i + 4 * j;
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c], acc[c + 1]);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
+              const uint32_t l = *reinterpret_cast<const uint32_t*>(&lo), h = *reinterpret_cast<const uint32_t*>(&hi);
+              w[j] = static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(l), s), __fdiv_rn(bf16hi(l), s))) |
+                     (static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(h), s), __fdiv_rn(bf16hi(h), s))) << 16);
+            }
+            *reinterpret_cast<uint4*>(qrow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = s;
+          }
+        }
+      } else {
+        float* prow = p.Cpart + (static_cast<int64_t>(c.split) * p.M + gm) * p.N + col0;
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i)
+          *reinterpret_cast<float4*>(prow + 4 * i) = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+// Adds the fp32 split-K partials in split order, rounds to bf16 and,
+// optionally, quantises each 128-column group of the bf16 result exactly as
+// the activation quantiser does.  One warp per 128-column group of a row.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int N,
+                                                            uint16_t* __restrict__ C, uint8_t* __restrict__ Cq,
+                                                            float* __restrict__ sCq) {
+  const int64_t groups = static_cast<int64_t>(M) * (N / 128);
+  const int lane = threadIdx.x & 31;
+  for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; g < groups;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x / 32) {
+    const int64_t r = g / (N / 128), cg = g % (N / 128);
+    const int64_t off = r * N + cg * 128 + lane * 4;
+    float4 a = *reinterpret_cast<const float4*>(part + off);
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(s) * M * N + off);
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&lo);
+    v.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(C + off) = v;
+    if (Cq != nullptr) {
+      const float s = group_scale(warp_max(fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
+                                                 fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))))));
+      const uint32_t q = e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s)) |
+                         (static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s))) << 16);
+      *reinterpret_cast<uint32_t*>(Cq + off) = q;
+      if (lane == 0) sCq[cg * M + r] = s;
+    }
+  }
+}
+
+}  // namespace bfp8

@@ -1,0 +1,193 @@
+"""torch-facing wrappers of the C ABI (argument marshalling only).
+
+Every function checks dtypes/shapes of the torch tensors it is given,
+allocates missing outputs with torch on the input's device, passes raw
+pointers and the current CUDA stream to libbfp8.so and raises
+``BFP8Error`` on a non-OK status.  All arithmetic happens in the CUDA
+kernels behind the ABI.
+
+Layouts are those of include/bfp8.h: E4M3 codes are torch.uint8 tensors,
+scales are float32, activation scales are group-major ([K/128, M] for a
+[M, K] tensor quantised along K).
+"""
+
+import torch
+
+from . import _lib
+
+FPROP, DGRAD, WGRAD = 0, 1, 2
+
+
+class BFP8Error(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        lib = _lib.load()
+        super().__init__(f"{what}: {_lib.STATUS.get(status, status)} ({lib.bfp8_status_string(status).decode()})")
+
+
+def _check(status, what):
+    if status != 0:
+        raise BFP8Error(status, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+    return t
+
+
+def _out(t, dtype, shape, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _need(t, dtype, shape, name)
+
+
+def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=None, stream=None):
+    """Quantise bf16 x [M, K] in 1x128 groups.
+
+    rows   -> q [M, K] uint8 (groups along K), s [K/128, M] float32
+    tokens -> qT [K, M] uint8 (groups of 128 tokens per column), sT [M/128, K]
+    Returns (q, s, qT, sT) with None for outputs not requested.
+    """
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    if rows:
+        q = _out(q, torch.uint8, (M, K), x.device, "q")
+        s = _out(s, torch.float32, (K // 128, M), x.device, "s")
+    else:
+        q = s = None
+    if tokens:
+        qT = _out(qT, torch.uint8, (K, M), x.device, "qT")
+        sT = _out(sT, torch.float32, (M // 128, K), x.device, "sT")
+    else:
+        qT = sT = None
+    lib = _lib.load()
+    _check(lib.bfp8_quantize_act_1x128(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _stream(stream)),
+           "quantize_act_1x128")
+    return q, s, qT, sT
+
+
+def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, stream=None):
+    """Quantise bf16 w [N, K] in 128x128 blocks -> (q [N, K], qT [K, N], s [N/128, K/128])."""
+    N, K = w.shape
+    _need(w, torch.bfloat16, (N, K), "w")
+    q = _out(q, torch.uint8, (N, K), w.device, "q") if want_q else None
+    qT = _out(qT, torch.uint8, (K, N), w.device, "qT") if want_qT else None
+    s = _out(s, torch.float32, (N // 128, K // 128), w.device, "s")
+    lib = _lib.load()
+    _check(lib.bfp8_quantize_w_128x128(_ptr(w), N, K, _ptr(q), _ptr(qT), _ptr(s), _stream(stream)),
+           "quantize_w_128x128")
+    return q, qT, s
+
+
+def gemm_workspace_bytes(layout, M, N, K):
+    return int(_lib.load().bfp8_gemm_workspace_bytes(layout, M, N, K))
+
+
+def fp8_block_gemm(layout, A, sa, B, sb, C=None, fused_quant=False, Cq=None, sCq=None, workspace=None, stream=None):
+    """Block-scaled GEMM C [M, N] = sum_kb (A . B^T)_kb * sa * sb, bf16 out.
+
+    A uint8 [M, K], B uint8 [N, K], sa float32 [K/128, M]; sb per layout:
+    FPROP [N/128, K/128], DGRAD [K/128, N/128], WGRAD [K/128, N].
+    With fused_quant also returns the E4M3 codes of C (groups along N).
+    Returns C or (C, Cq, sCq).
+    """
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, torch.uint8, (M, K), "A")
+    _need(B, torch.uint8, (N, K), "B")
+    _need(sa, torch.float32, (K // 128, M), "sa")
+    sb_shape = {FPROP: (N // 128, K // 128), DGRAD: (K // 128, N // 128), WGRAD: (K // 128, N)}[layout]
+    _need(sb, torch.float32, sb_shape, "sb")
+    C = _out(C, torch.bfloat16, (M, N), A.device, "C")
+    if fused_quant:
+        Cq = _out(Cq, torch.uint8, (M, N), A.device, "Cq")
+        sCq = _out(sCq, torch.float32, (N // 128, M), A.device, "sCq")
+    else:
+        Cq = sCq = None
+    need = gemm_workspace_bytes(layout, M, N, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    _check(lib.bfp8_fp8_block_gemm(layout, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb), M, N, K, _ptr(C), _ptr(Cq),
+                                   _ptr(sCq), _ptr(workspace), ws_bytes, _stream(stream)), "fp8_block_gemm")
+    return (C, Cq, sCq) if fused_quant else C
+
+
+def linear_fwd_workspace_bytes(M, N, K):
+    return int(_lib.load().bfp8_linear_fwd_workspace_bytes(M, N, K))
+
+
+def linear_bwd_workspace_bytes(M, N, K):
+    return int(_lib.load().bfp8_linear_bwd_workspace_bytes(M, N, K))
+
+
+def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None):
+    """Y = X . W^T through the fused forward.  Returns (Y, saved) where saved
+    holds WqT, sW, XqT, sXT for linear_bwd."""
+    M, K = X.shape
+    N = W.shape[0]
+    _need(X, torch.bfloat16, (M, K), "X")
+    _need(W, torch.bfloat16, (N, K), "W")
+    dev = X.device
+    Y = _out(Y, torch.bfloat16, (M, N), dev, "Y")
+    if saved is None:
+        saved = dict(WqT=torch.empty((K, N), dtype=torch.uint8, device=dev),
+                     sW=torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
+                     XqT=torch.empty((K, M), dtype=torch.uint8, device=dev),
+                     sXT=torch.empty((M // 128, K), dtype=torch.float32, device=dev))
+    if workspace is None:
+        workspace = torch.empty(linear_fwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    lib = _lib.load()
+    _check(lib.bfp8_linear_fwd(_ptr(X), _ptr(W), M, N, K, _ptr(Y), _ptr(saved["WqT"]), _ptr(saved["sW"]),
+                               _ptr(saved["XqT"]), _ptr(saved["sXT"]), _ptr(workspace), workspace.numel(),
+                               _stream(stream)), "linear_fwd")
+    return Y, saved
+
+
+def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None):
+    """(dX, dW) for the layer whose forward produced ``saved``."""
+    M, N = dY.shape
+    K = saved["WqT"].shape[0]
+    _need(dY, torch.bfloat16, (M, N), "dY")
+    _need(saved["WqT"], torch.uint8, (K, N), "WqT")
+    _need(saved["sW"], torch.float32, (N // 128, K // 128), "sW")
+    _need(saved["XqT"], torch.uint8, (K, M), "XqT")
+    _need(saved["sXT"], torch.float32, (M // 128, K), "sXT")
+    dev = dY.device
+    dX = _out(dX, torch.bfloat16, (M, K), dev, "dX")
+    dW = _out(dW, torch.bfloat16, (N, K), dev, "dW")
+    if workspace is None:
+        workspace = torch.empty(linear_bwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    lib = _lib.load()
+    _check(lib.bfp8_linear_bwd(_ptr(dY), _ptr(saved["WqT"]), _ptr(saved["sW"]), _ptr(saved["XqT"]),
+                               _ptr(saved["sXT"]), M, N, K, _ptr(dX), _ptr(dW), _ptr(workspace), workspace.numel(),
+                               _stream(stream)), "linear_bwd")
+    return dX, dW
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and return the device-side status code (0 = ok)."""
+    return int(_lib.load().bfp8_sync_status(_stream(stream)))
+
+
+def set_wait_limit_ns(ns):
+    _check(_lib.load().bfp8_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
+
+
+def set_gemm_splits(splits):
+    _check(_lib.load().bfp8_set_gemm_splits(int(splits)), "set_gemm_splits")

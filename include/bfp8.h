@@ -1,0 +1,201 @@
+/*
+ * bfp8.h -- C ABI of the blockwise-FP8 Transformer linear layer for B300 (sm_103a).
+ *
+ * What the library computes is the linear-layer numerics of "Puro-2B: Poor
+ * Lab's Qwen2-1.5B Trained on RTX 5090 within $5090" (papers.lianghsun.dev
+ * translation), section 3.2 "FP8 mixed-precision training":
+ *   - linear-layer GEMM operands are E4M3 (Micikevicius et al. 2022 format);
+ *   - activations and activation gradients are quantised in 1-D groups of 128
+ *     consecutive values along the GEMM reduction dimension;
+ *   - weights are quantised in 2-D 128x128 blocks;
+ *   - every group/block scale is computed online from that group's values.
+ * The decoded value of a code is code * scale (bloombook.cn tutorial, MXFP
+ * figure, "V_i = Q_i x X"), so every scale below is a dequantisation
+ * multiplier.  The scale value is amax/448 in fp32 (1.0 for an all-zero
+ * group) and codes are E4M3(x / scale) rounded to nearest-even with
+ * saturation to +-448.
+ *
+ * Conventions for every entry point
+ *   - All matrices are row-major and contiguous.  "bf16" is IEEE bfloat16.
+ *   - Every dimension must be a positive multiple of 128 (BFP8_EINVAL).
+ *   - Every device pointer must be 16-byte aligned (BFP8_EALIGN).
+ *   - The caller owns all memory.  The library allocates no device memory
+ *     and keeps no state between calls except a per-device error word and
+ *     cached device attributes.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  The return value reports argument and
+ *     launch errors only; bfp8_sync_status() reports errors raised on the
+ *     device (an expired bounded wait).
+ *   - Input and output buffers must not overlap.
+ *
+ * Scale layouts ("group-major": the scales of one group index are contiguous)
+ *   - 1x128 groups along the columns of an [R, C] tensor: s is [C/128, R],
+ *     s[g*R + r] scales elements (r, 128g .. 128g+127).
+ *   - 128x128 weight blocks of W [N, K]: s is [N/128, K/128].
+ */
+#ifndef BFP8_H
+#define BFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* bfp8_stream_t;
+
+typedef enum {
+  BFP8_OK = 0,
+  BFP8_EINVAL = 1,       /* null pointer, bad enum, or a dimension that is not a positive multiple of 128 */
+  BFP8_EALIGN = 2,       /* a pointer is not 16-byte aligned */
+  BFP8_EUNSUPPORTED = 3, /* no usable sm_103a device, or a size beyond what a kernel indexes */
+  BFP8_ECUDA = 4,        /* a CUDA runtime or driver call failed (launch, tensor-map encode, sync) */
+  BFP8_ETIMEOUT = 5,     /* a device-side bounded wait expired; reported by bfp8_sync_status */
+  BFP8_EWORKSPACE = 6    /* workspace pointer null or smaller than the matching *_workspace_bytes() */
+} bfp8_status;
+
+/* The three GEMMs of a linear layer Y = X . W^T with X [tokens, in], W [out, in]. */
+typedef enum {
+  BFP8_FPROP = 0, /* Y  = X  . W^T : reduction over in-features  */
+  BFP8_DGRAD = 1, /* dX = dY . W   : reduction over out-features */
+  BFP8_WGRAD = 2  /* dW = dY^T . X : reduction over tokens       */
+} bfp8_layout;
+
+/*
+ * Activation / activation-gradient quantiser, 1x128 groups (section 3.2:
+ * groups of 128 consecutive values along the GEMM reduction dimension).
+ *
+ *   x   bf16 [M, K], read only.
+ *   q   E4M3 [M, K] or NULL: groups of 128 along K (the fprop operand for an
+ *       activation, the dgrad operand for an output gradient).
+ *   s   fp32 [K/128, M]: scales of q; required when q is given, else ignored.
+ *   qT  E4M3 [K, M] or NULL: groups of 128 consecutive rows (tokens) of x per
+ *       column, stored transposed so each group is contiguous (the wgrad
+ *       operand, where the reduction runs over tokens).
+ *   sT  fp32 [M/128, K]: scales of qT; required when qT is given.
+ * At least one of q / qT must be given.  Both outputs come from a single
+ * read of x.  Errors: EINVAL, EALIGN, ECUDA.
+ */
+bfp8_status bfp8_quantize_act_1x128(const void* x, int64_t M, int64_t K,
+                                    uint8_t* q, float* s,
+                                    uint8_t* qT, float* sT,
+                                    bfp8_stream_t stream);
+
+/*
+ * Weight quantiser, 128x128 blocks (section 3.2: weights use 2-D 128x128
+ * blocks).  A block is the same set of values in W and W^T, so one scale
+ * array serves fprop (W) and dgrad (W^T).
+ *
+ *   w   bf16 [N, K], read only.
+ *   q   E4M3 [N, K] or NULL (fprop operand).
+ *   qT  E4M3 [K, N] or NULL (dgrad operand, = q transposed).
+ *   s   fp32 [N/128, K/128], required.
+ * At least one of q / qT must be given.  Errors: EINVAL, EALIGN, ECUDA.
+ */
+bfp8_status bfp8_quantize_w_128x128(const void* w, int64_t N, int64_t K,
+                                    uint8_t* q, uint8_t* qT, float* s,
+                                    bfp8_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with fp32 promotion per 128-deep slice (section 3.2:
+ * E4M3 operands, fp32 training state; scales per 1x128 group / 128x128 block).
+ *
+ *   C[i, j] = bf16( sum over slices kb of  P_kb[i, j] * sa(i, kb) * sb(j, kb) )
+ *   P_kb[i, j] = sum_{k in slice kb} A[i, k] * B[j, k]   (tensor-core fp32 accumulation)
+ *
+ * M, N: output rows and columns; K: reduction length.  A E4M3 [M, K] and
+ * B E4M3 [N, K] are both K-contiguous.  sa is fp32 [K/128, M] for every
+ * layout.  sb depends on the layout:
+ *   FPROP: A = Xq,   B = Wq  [N, K]: sb = sW  [N/128, K/128] (weight blocks)
+ *   DGRAD: A = dYq,  B = WqT [N, K]: sb = sW  [K/128, N/128] (the same weight
+ *          scales, whose block rows now run along the reduction)
+ *   WGRAD: A = dYqT, B = XqT [N, K]: sb = sXT [K/128, N]     (token groups)
+ *   C    bf16 [M, N], written.
+ *   Cq / sCq  optional fused quantised epilogue: E4M3 [M, N] codes of the
+ *        bf16 C in 1x128 groups along N, with fp32 scales [N/128, M], exactly
+ *        as bfp8_quantize_act_1x128 would produce from C.  Both or neither.
+ *   workspace / ws_bytes  scratch of at least bfp8_gemm_workspace_bytes()
+ *        bytes (may be 0 bytes, then workspace may be NULL).
+ * Errors: EINVAL, EALIGN, EWORKSPACE, EUNSUPPORTED, ECUDA.
+ */
+bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout,
+                                const uint8_t* A, const float* sa,
+                                const uint8_t* B, const float* sb,
+                                int64_t M, int64_t N, int64_t K,
+                                void* C, uint8_t* Cq, float* sCq,
+                                void* workspace, size_t ws_bytes,
+                                bfp8_stream_t stream);
+
+/* Scratch bytes bfp8_fp8_block_gemm needs for these arguments (0 when none). */
+size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Fused forward of one linear layer, Y [M, N] = X [M, K] . W [N, K]^T
+ * (section 3.2: W stays bf16/fp32 and is re-quantised on every use; FP8 is
+ * the online compute and activation-storage format).  Runs the weight
+ * quantiser, the dual activation quantiser and the FPROP GEMM.
+ *
+ *   X bf16 [M, K], W bf16 [N, K]: inputs.   Y bf16 [M, N]: output.
+ *   Saved for the backward pass, caller-owned outputs:
+ *     WqT E4M3 [K, N], sW fp32 [N/128, K/128], XqT E4M3 [K, M], sXT fp32 [M/128, K].
+ *   ws / ws_bytes: scratch of at least bfp8_linear_fwd_workspace_bytes().
+ * Errors: as the calls it makes.
+ */
+bfp8_status bfp8_linear_fwd(const void* X, const void* W,
+                            int64_t M, int64_t N, int64_t K,
+                            void* Y,
+                            uint8_t* WqT, float* sW, uint8_t* XqT, float* sXT,
+                            void* ws, size_t ws_bytes,
+                            bfp8_stream_t stream);
+size_t bfp8_linear_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Fused backward of the same layer: quantises dY [M, N] along N (dgrad) and
+ * along tokens (wgrad) in one pass, then runs DGRAD (dX [M, K]) and WGRAD
+ * (dW [N, K]) with the tensors saved by bfp8_linear_fwd.
+ *   dX, dW: bf16 outputs.  ws / ws_bytes: scratch of at least
+ *   bfp8_linear_bwd_workspace_bytes().
+ */
+bfp8_status bfp8_linear_bwd(const void* dY,
+                            const uint8_t* WqT, const float* sW,
+                            const uint8_t* XqT, const float* sXT,
+                            int64_t M, int64_t N, int64_t K,
+                            void* dX, void* dW,
+                            void* ws, size_t ws_bytes,
+                            bfp8_stream_t stream);
+size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns BFP8_ETIMEOUT if a kernel's bounded wait expired since the
+ * last call (that kernel's outputs are then undefined), BFP8_ECUDA if the
+ * synchronisation failed, else BFP8_OK.
+ */
+bfp8_status bfp8_sync_status(bfp8_stream_t stream);
+
+/*
+ * Sets the limit, in nanoseconds, of every device-side wait the kernels make
+ * on the current device from now on (default 2e9).  Used by tests to make a
+ * wait expire on purpose; 0 restores the default.
+ */
+bfp8_status bfp8_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Overrides the split-K factor the GEMM picks (0 restores the automatic
+ * choice, which splits the reduction only when that fills idle SMs at a
+ * lower cost than the extra fp32 partial traffic).  Applies to every later
+ * bfp8_fp8_block_gemm / linear call in the process and to the matching
+ * *_workspace_bytes() results; the factor is capped at K/128.
+ */
+bfp8_status bfp8_set_gemm_splits(int splits);
+
+/* Static description of a status code. */
+const char* bfp8_status_string(bfp8_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BFP8_H */

@@ -1,0 +1,104 @@
+"""GPU quantisers vs the CPU oracle: E4M3 codes and fp32 scales bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (assert_codes_equal, assert_scales_equal, bf16_input, dev, np32, u8, to_gpu)
+from oracle import quant
+from blockwise_fp8_linear_quantise_b300 import ops, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def check_act(x_bf16):
+    x = x_bf16.to(dev())
+    q, s, qT, sT = ops.quantize_act_1x128(x, rows=True, tokens=True)
+    torch.cuda.synchronize()
+    assert ops.sync_status() == 0
+    xn = np32(x_bf16)
+    oq, os_ = quant.quantize_act_1x128(xn)
+    oqT, osT = quant.quantize_act_tokens_1x128(xn)
+    assert_codes_equal(u8(q), oq, "q")
+    assert_scales_equal(s.cpu().numpy(), os_, "s")
+    assert_codes_equal(u8(qT), oqT, "qT")
+    assert_scales_equal(sT.cpu().numpy(), osT, "sT")
+    # single-output variants give the same bytes
+    q2, s2, _, _ = ops.quantize_act_1x128(x, rows=True, tokens=False)
+    _, _, qT2, sT2 = ops.quantize_act_1x128(x, rows=False, tokens=True)
+    assert torch.equal(q2, q) and torch.equal(s2, s) and torch.equal(qT2, qT) and torch.equal(sT2, sT)
+
+
+def check_w(w_bf16):
+    w = w_bf16.to(dev())
+    q, qT, s = ops.quantize_w_128x128(w)
+    assert ops.sync_status() == 0
+    oq, oqT, os_ = quant.quantize_w_128x128(np32(w_bf16))
+    assert_codes_equal(u8(q), oq, "Wq")
+    assert_codes_equal(u8(qT), oqT, "WqT")
+    assert_scales_equal(s.cpu().numpy(), os_, "sW")
+    q1, _, s1 = ops.quantize_w_128x128(w, want_qT=False)
+    _, qT1, _ = ops.quantize_w_128x128(w, want_q=False)
+    assert torch.equal(q1, q) and torch.equal(qT1, qT) and torch.equal(s1, s)
+
+
+def test_tiny_config():
+    check_act(bf16_input("tiny", "x"))
+    check_w(bf16_input("tiny", "w"))
+
+
+@pytest.mark.parametrize("M,K", [(128, 128), (384, 640), (1152, 256)])
+def test_multi_tile_shapes(M, K):
+    rng = np.random.default_rng(M * 7 + K)
+    x = workloads.to_bf16(rng.standard_normal((M, K)).astype(np.float32) * np.exp2(rng.integers(-20, 20, (M, 1))))
+    check_act(x)
+    check_w(x)
+
+
+def test_edge_values():
+    # zeros (scale 1), signed zeros, subnormal-scale groups, huge groups, ties
+    M, K = 256, 384
+    x = np.zeros((M, K), np.float32)
+    x[1, :] = -0.0
+    x[2, 5] = 1e-38                       # amax bf16-subnormal-ish: scale is an fp32 subnormal
+    x[2, 6] = -3e-39
+    x[3, :] = 3.0e38                      # near bf16 max
+    x[3, 7] = -1.0
+    x[4, :128] = np.float32(17.0 / 128)   # 17 -> tie between 16 and 18 after scaling by amax 3.5
+    x[4, 0] = 3.5
+    x[5:, :] = np.random.default_rng(0).standard_normal((M - 5, K)).astype(np.float32)
+    x[200:210, 128:256] = 0.0             # zero token group
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    fin = bits[np.isfinite(bits)]
+    x[128:256, 256:384].flat[: min(fin.size, 128 * 128)] = fin[: 128 * 128]
+    xb = workloads.to_bf16(x)
+    check_act(xb)
+    check_w(xb)
+
+
+def test_every_bf16_bit_pattern():
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    fin = bits[np.isfinite(bits)]
+    x = np.zeros((512, 256), np.float32)
+    x.flat[: fin.size] = fin
+    xb = workloads.to_bf16(x)
+    check_act(xb)
+    check_w(xb)
+
+
+@pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_gateup", "w"), ("mlp_down", "x"),
+                                      ("mlp_down", "w"), ("mlp_down", "dy"), ("attn_proj", "x"),
+                                      ("attn_proj", "w_qkv"), ("attn_proj", "dy_qkv")])
+def test_full_size_configs(name, tag):
+    t = bf16_input(name, tag)
+    if tag.startswith("w"):
+        check_w(t)
+    else:
+        check_act(t)
+
+
+def test_stack_layer_tensors():
+    wl = workloads.make("stack28")
+    check_act(workloads.tensor(wl, "x_f"))
+    check_act(workloads.tensor(wl, "dy_gu"))
+    check_w(workloads.tensor(wl, "w_gu", layer=27))
