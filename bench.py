@@ -1,0 +1,609 @@
+#!/usr/bin/env python3
+"""Benchmark of the blockwise-FP8 Transformer linear layer on B300.
+
+One step is one training micro-step of a stack of blockwise-FP8 linear
+layers: for every linear, forward (weight quantisation in 128x128 blocks,
+activation quantisation in 1x128 groups along features and along tokens,
+FPROP GEMM), then, in reverse order, backward (output-gradient quantisation
+along features and along tokens, DGRAD and WGRAD GEMMs).  This is the linear
+numerics of "Puro-2B: Poor Lab's Qwen2-1.5B Trained on RTX 5090 within
+$5090", section 3.2, on synthetic inputs shaped like its layers (hidden 2048,
+FFN 6144, 16 query + 8 KV heads of dim 128, 4 x 4096 tokens).
+
+Arms
+  default          the CUDA kernels behind libbfp8.so, inputs resident in HBM;
+                   also reports
+                     e2e           the same step through the public fused calls
+                                   (linear_fwd / linear_bwd) with every input
+                                   copied from pinned host memory and every
+                                   weight gradient copied back, inside the
+                                   timed region;
+                     roofline      GEMM TFLOP/s against the FP8 tensor peak and
+                                   quantiser GB/s against HBM bandwidth, from
+                                   CUDA events around every call;
+                     cpu_baseline  the CPU oracle timed on a bounded sample.
+  --impl reference the CPU oracle on a bounded sample of the same workload
+                   (this method has no other implementation to run).
+
+The printed value is whole-job GEMM throughput: 2*M*N*K FLOPs of every FPROP,
+DGRAD and WGRAD GEMM of the step, divided by the step time (quantisers
+included).  Launch with N processes (torchrun) to run N independent replicas;
+no data crosses between them.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "blockwise-FP8 GEMM TFLOP/s (fwd+dgrad+wgrad) and % of B300 FP8 dense peak"
+UNIT = "TFLOP/s"
+
+# Fallback denominators (one earlier B300 measurement), used only when the
+# measured-peaks file is absent.
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
+
+# DRAM traffic per launch from an ncu capture, valid only for the kernel
+# sources whose hash is recorded with it (see kernel_source_hash()).
+TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("common.cuh", "gemm.cuh", "quant.cuh", "api.cu"):
+        with open(os.path.join(ROOT, "blockwise_fp8_linear_quantise_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- host logic
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
+    ap.add_argument("--workload", default="stack28",
+                    choices=("tiny", "mlp_gateup", "mlp_down", "attn_proj", "stack28"))
+    ap.add_argument("--layers", type=int, default=28, help="stack28 only: layers to run (profiling cases)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=512)
+    ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_group(world):
+    """A gloo group for the barrier and the max over ranks (host tensors
+    only: the replicas exchange no data)."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist.group.WORLD
+
+
+def barrier(group):
+    if group is not None:
+        import torch.distributed as dist
+        dist.barrier(group)
+
+
+def max_over_ranks(x, group):
+    if group is None:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def sum_over_ranks(x, group):
+    if group is None:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def linear_list(wl, layers):
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    specs = []
+    for s in wl.linears:
+        li = workloads.layer_of(s)
+        if li is None or li < layers:
+            specs.append(s)
+    return specs
+
+
+def gemm_flops(specs):
+    return sum(2 * s.M * s.N * s.K * (3 if s.backward else 1) for s in specs)
+
+
+def workload_config(wl, specs, layers):
+    cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M,
+           "shapes_MNK": sorted({(s.M, s.N, s.K) for s in specs}),
+           "passes": "fprop+dgrad+wgrad" if specs[0].backward else "fprop",
+           "l2": "inputs larger than L2: each step streams several GB through HBM (no explicit flush)",
+           "parallelism": "replicas (one independent step per GPU)"}
+    if wl.name == "stack28":
+        cfg["layers"] = layers
+        cfg["what"] = ("Puro-2B linear stack, one micro-step: per layer QKV 2048->4096, O 2048->2048, "
+                       "gate+up 2048->12288, down 6144->2048 on 16384 tokens; activations and output gradients "
+                       "N(0,1) with 0.1% x50 outliers, weights N(0,0.02^2), distinct per layer")
+    return cfg
+
+
+def summarise_clocks(rows):
+    """rows: parsed nvidia-smi samples -> the clocks object of the JSON line."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    sm = [r["sm"] for r in rows if r["sm"] is not None]
+    reasons = set()
+    for r in rows:
+        reasons.update(r["active"])
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(r["sm_max"] for r in rows if r["sm_max"] is not None) if sm else None,
+            "power_w_max": max((r["power"] for r in rows if r["power"] is not None), default=None),
+            "reasons": sorted(reasons), "samples": len(rows)}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons while the
+    timed region runs."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None or self.gpu_id is None:
+            return
+        self.proc = subprocess.Popen(
+            [exe, "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+             "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+    def stop(self):
+        if self.proc is None:
+            return summarise_clocks([])
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+
+            def num(v):
+                try:
+                    return float(v)
+                except ValueError:
+                    return None
+            rows.append({"sm": num(parts[0]), "sm_max": num(parts[1]), "power": num(parts[2]),
+                         "active": [n for n, v in zip(self.NAMES, parts[3:]) if v.lower() == "active"]})
+        return summarise_clocks(rows)
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_sample(wl, specs, tokens):
+    """CPU inputs for a bounded oracle sample: the first `tokens` tokens of
+    every distinct linear shape of the workload's first layer, drawn from the
+    workload's own distributions."""
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    seen, sample = set(), []
+    for s in specs:
+        key = (s.N, s.K, s.backward)
+        if key in seen:
+            continue
+        seen.add(key)
+        m = min(tokens, s.M)
+        f = lambda tag, shape: workloads.to_bf16(
+            workloads.draw(wl.dists[tag], shape, wl.seed, tag + "#cpu-sample")).float().numpy()
+        x = f(s.x_tag, (m, s.K))
+        w = f(s.w_tag, (s.N, s.K))
+        dy = f(s.dy_tag, (m, s.N)) if s.backward else None
+        sample.append((x, w, dy))
+    return sample
+
+
+def run_oracle(sample):
+    """Oracle linear forward (+ backward) over the sample; returns GEMM FLOPs."""
+    from oracle import gemm as ogemm
+    flops = 0
+    for x, w, dy in sample:
+        _, saved = ogemm.linear_fwd(x, w)
+        flops += 2 * x.shape[0] * w.shape[0] * x.shape[1]
+        if dy is not None:
+            ogemm.linear_bwd(dy, saved)
+            flops += 4 * x.shape[0] * w.shape[0] * x.shape[1]
+    return flops
+
+
+def describe_sample(sample):
+    return "; ".join(f"M={x.shape[0]} N={w.shape[0]} K={x.shape[1]} {'fwd+bwd' if dy is not None else 'fwd'}"
+                     for x, w, dy in sample)
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    wl = workloads.make(args.workload)
+    specs = linear_list(wl, args.layers)
+    sample = oracle_sample(wl, specs, args.ref_sample_tokens)
+    for _ in range(args.warmup):
+        run_oracle(sample)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += run_oracle(sample)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = cpu_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
+            "data": "synthetic", "config": workload_config(wl, specs, args.layers),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + describe_sample(sample)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------- GPU runner
+class StackRunner:
+    """Device buffers and the per-step call sequence of a workload.
+
+    The step is issued as the C ABI's component calls (the same kernels, in
+    the same order, as bfp8_linear_fwd / bfp8_linear_bwd) so that CUDA events
+    can separate the quantiser and GEMM time.  Arguments are marshalled once;
+    a step only makes the ctypes calls.
+    """
+
+    def __init__(self, wl, specs, dev):
+        import torch
+        from blockwise_fp8_linear_quantise_b300 import _lib, ops, workloads
+        self.torch = torch
+        self.lib = _lib.load()
+        self.ops = ops
+        self.specs = specs
+        self.dev = dev
+        u8, f32, bf16 = torch.uint8, torch.float32, torch.bfloat16
+        E = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+
+        # inputs
+        self.inputs = {}
+        device_draw = wl.name == "stack28"
+        for s in specs:
+            li = workloads.layer_of(s)
+            for tag, layer in ((s.x_tag, None), (s.w_tag, li), (s.dy_tag if s.backward else None, None)):
+                if tag is None or (tag, layer) in self.inputs:
+                    continue
+                t = (workloads.tensor_cuda(wl, tag, layer, device=dev) if device_draw
+                     else workloads.tensor(wl, tag, layer).to(dev))
+                self.inputs[(tag, layer)] = t.contiguous()
+
+        # scratch per shape, saved tensors and weight gradients per linear
+        self.scratch = {}
+        self.saved, self.dW = [], []
+        ws = 0
+        for s in specs:
+            M, N, K = s.M, s.N, s.K
+            key = (M, N, K)
+            if key not in self.scratch:
+                self.scratch[key] = dict(Wq=E((N, K), u8), Xq=E((M, K), u8), sX=E((K // 128, M), f32),
+                                         Y=E((M, N), bf16), dYq=E((M, N), u8), sdY=E((N // 128, M), f32),
+                                         dYqT=E((N, M), u8), sdYT=E((M // 128, N), f32), dX=E((M, K), bf16))
+            self.saved.append(dict(WqT=E((K, N), u8), sW=E((N // 128, K // 128), f32),
+                                   XqT=E((K, M), u8), sXT=E((M // 128, K), f32)))
+            self.dW.append(E((N, K), bf16) if s.backward else None)
+            ws = max(ws, ops.gemm_workspace_bytes(ops.FPROP, M, N, K))
+            if s.backward:
+                ws = max(ws, ops.gemm_workspace_bytes(ops.DGRAD, M, K, N),
+                         ops.gemm_workspace_bytes(ops.WGRAD, N, K, M),
+                         ops.linear_bwd_workspace_bytes(M, N, K))
+            ws = max(ws, ops.linear_fwd_workspace_bytes(M, N, K))
+        self.ws = E((max(ws, 256),), u8)
+        self.ws_bytes = self.ws.numel()
+        self._marshal()
+
+    def _marshal(self):
+        """Argument tuples of every ABI call of one step, with their kind and
+        algorithmic work (FLOPs for GEMMs, bytes for quantisers)."""
+        P = lambda t: None if t is None else t.data_ptr()
+        lib = self.lib
+        fwd, bwd = [], []
+        for i, s in enumerate(self.specs):
+            M, N, K = s.M, s.N, s.K
+            sc, sv = self.scratch[(M, N, K)], self.saved[i]
+            X = self.inputs[(s.x_tag, None)]
+            from blockwise_fp8_linear_quantise_b300 import workloads
+            W = self.inputs[(s.w_tag, workloads.layer_of(s))]
+            ne_w, ne_x = N * K, M * K
+            fwd.append(("quant_w", ne_w * (4 + 4 / 16384), lib.bfp8_quantize_w_128x128,
+                        (P(W), N, K, P(sc["Wq"]), P(sv["WqT"]), P(sv["sW"]))))
+            fwd.append(("quant_act", ne_x * (4 + 8 / 128), lib.bfp8_quantize_act_1x128,
+                        (P(X), M, K, P(sc["Xq"]), P(sc["sX"]), P(sv["XqT"]), P(sv["sXT"]))))
+            fwd.append(("fprop", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
+                        (self.ops.FPROP, P(sc["Xq"]), P(sc["sX"]), P(sc["Wq"]), P(sv["sW"]), M, N, K, P(sc["Y"]),
+                         None, None, P(self.ws), self.ws_bytes)))
+            if s.backward:
+                dY = self.inputs[(s.dy_tag, None)]
+                ne_y = M * N
+                b = [("quant_act", ne_y * (4 + 8 / 128), lib.bfp8_quantize_act_1x128,
+                      (P(dY), M, N, P(sc["dYq"]), P(sc["sdY"]), P(sc["dYqT"]), P(sc["sdYT"]))),
+                     ("dgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
+                      (self.ops.DGRAD, P(sc["dYq"]), P(sc["sdY"]), P(sv["WqT"]), P(sv["sW"]), M, K, N, P(sc["dX"]),
+                       None, None, P(self.ws), self.ws_bytes)),
+                     ("wgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
+                      (self.ops.WGRAD, P(sc["dYqT"]), P(sc["sdYT"]), P(sv["XqT"]), P(sv["sXT"]), N, K, M,
+                       P(self.dW[i]), None, None, P(self.ws), self.ws_bytes))]
+                bwd.append(b)
+        self.calls = fwd + [c for b in reversed(bwd) for c in b]
+
+    def step(self, marks=None):
+        """One micro-step on the current stream.  With `marks`, records a
+        CUDA event after every call: marks gets [(event, kind, work), ...]
+        starting with (event, None, 0)."""
+        torch = self.torch
+        stream = torch.cuda.current_stream().cuda_stream
+        if marks is not None:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            marks.append((e, None, 0))
+        for kind, work, fn, args in self.calls:
+            st = fn(*args, stream)
+            if st != 0:
+                raise RuntimeError(f"{kind}: status {st}")
+            if marks is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                marks.append((e, kind, work))
+
+    # ------------------------------------------------------------ e2e arm
+    def e2e_setup(self):
+        """Pinned host copies of every input; pinned host buffers for the
+        weight gradients."""
+        torch = self.torch
+        self.h_inputs = {k: v.cpu().pin_memory() for k, v in self.inputs.items()}
+        self.h_dW = [None if d is None else torch.empty(d.shape, dtype=d.dtype, pin_memory=True) for d in self.dW]
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.h_inputs.values())
+        self.d2h_bytes = sum(d.numel() * d.element_size() for d in self.dW if d is not None)
+        if not any(s.backward for s in self.specs):
+            # forward-only workloads read back their outputs instead
+            self.d2h_bytes = sum(self.scratch[(s.M, s.N, s.K)]["Y"].numel() * 2 for s in self.specs)
+
+    def e2e_step(self):
+        """Host inputs -> device, fused public calls, weight gradients -> host."""
+        from blockwise_fp8_linear_quantise_b300 import workloads
+        ops = self.ops
+        for k, h in self.h_inputs.items():
+            self.inputs[k].copy_(h, non_blocking=True)
+        for i, s in enumerate(self.specs):
+            X = self.inputs[(s.x_tag, None)]
+            W = self.inputs[(s.w_tag, workloads.layer_of(s))]
+            Y = self.scratch[(s.M, s.N, s.K)]["Y"]
+            ops.linear_fwd(X, W, Y=Y, saved=self.saved[i], workspace=self.ws)
+            if not s.backward:
+                Y.cpu()  # forward-only: the output is the step's result
+        for i in reversed(range(len(self.specs))):
+            s = self.specs[i]
+            if not s.backward:
+                continue
+            dX = self.scratch[(s.M, s.N, s.K)]["dX"]
+            ops.linear_bwd(self.inputs[(s.dy_tag, None)], self.saved[i], dX=dX, dW=self.dW[i], workspace=self.ws)
+            self.h_dW[i].copy_(self.dW[i], non_blocking=True)
+
+
+def interval_stats(marks):
+    """Sum of event intervals per kind: {kind: [launch_calls, ms, work]}."""
+    out = {}
+    prev = None
+    for e, kind, work in marks:
+        if kind is not None and prev is not None:
+            ms = prev.elapsed_time(e)
+            d = out.setdefault(kind, [0, 0.0, 0.0])
+            d[0] += 1
+            d[1] += ms
+            d[2] += work
+        prev = e
+    return out
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def gpu_arm(args):
+    import torch
+    rank, world, local = dist_env()
+    group = init_group(world)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the kernels need an sm_103a GPU; there is no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from blockwise_fp8_linear_quantise_b300 import build as bld, ops, workloads
+    bld.build()
+    wl = workloads.make(args.workload)
+    layers = args.layers if args.workload == "stack28" else 0
+    specs = linear_list(wl, layers)
+    runner = StackRunner(wl, specs, dev)
+    flops_step = gemm_flops(specs)
+
+    # warm-up
+    for _ in range(args.warmup):
+        runner.step()
+    torch.cuda.synchronize()
+    if ops.sync_status() != 0:
+        raise SystemExit("device status not ok after warm-up")
+
+    # timed region
+    clocks = ClockSampler(gpu_uuid(dev))
+    barrier(group)
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = ops.launch_count()
+    marks = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        runner.step(marks)
+    t_end.record()
+    torch.cuda.synchronize()
+    launches = ops.launch_count() - launches0
+    clk = clocks.stop()
+    barrier(group)
+    st = ops.sync_status()
+    if st != 0:
+        raise SystemExit(f"device status {st} in the timed region")
+    ms_local = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms_local, group)
+    total_flops = sum_over_ranks(flops_step * args.steps, group)
+    value = total_flops / (ms * 1e-3) / 1e12
+    ms_per_step = ms / args.steps
+
+    stats = interval_stats(marks)
+    peaks, basis = load_peaks()
+    fp8_sust = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
+    g = [stats[k] for k in ("fprop", "dgrad", "wgrad") if k in stats]
+    g_calls = sum(x[0] for x in g)
+    g_ms = sum(x[1] for x in g)
+    g_flops = sum(x[2] for x in g)
+    g_achieved = g_flops / (g_ms * 1e-3) / 1e12
+    q = [stats[k] for k in ("quant_w", "quant_act") if k in stats]
+    q_ms = sum(x[1] for x in q)
+    q_bytes = sum(x[2] for x in q)
+    q_achieved = q_bytes / (q_ms * 1e-3) / 1e9 if q_ms > 0 else None
+    total_ms = sum(v[1] for v in stats.values())
+    src_hash = kernel_source_hash()
+    traffic = TRAFFIC.get(("gemm", args.workload, layers, src_hash))
+    per_kernel = {k: {"calls": v[0], "ms_total": round(v[1], 3), "share": round(v[1] / total_ms, 4),
+                      ("TFLOP/s" if k in ("fprop", "dgrad", "wgrad") else "GB/s"):
+                          round(v[2] / (v[1] * 1e-3) / (1e12 if k in ("fprop", "dgrad", "wgrad") else 1e9), 1)}
+                  for k, v in sorted(stats.items())}
+    roofline = {"bound": "tensor", "kernel": "block_gemm_kernel (+ split-K reduce where planned), all GEMM calls",
+                "achieved": round(g_achieved, 1), "peak": round(fp8_sust, 1), "unit": "TFLOP/s",
+                "frac": round(g_achieved / fp8_sust, 4),
+                "peak_basis": f"{FP8_PER_BF16:g} x {basis} bf16 sustained ({peaks['bf16_tflops_sustained']}) TFLOP/s",
+                "frac_of_burst": round(g_achieved / fp8_burst, 4),
+                "traffic": traffic, "flops_per_call": round(g_flops / max(g_calls, 1))}
+    roofline_q = None
+    if q_achieved is not None:
+        roofline_q = {"bound": "hbm", "kernel": "quantize_tile_kernel (activation dual + weight)",
+                      "achieved": round(q_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": round(q_achieved / peaks["hbm_gbs"], 4), "peak_basis": f"{basis} HBM copy",
+                      "bytes_per_call": round(q_bytes / max(sum(x[0] for x in q), 1)), "traffic": None}
+
+    # e2e through the public fused calls with host buffers
+    e2e = None
+    if not args.no_e2e:
+        runner.e2e_setup()
+        for _ in range(max(1, min(args.warmup, 2))):
+            runner.e2e_step()
+        torch.cuda.synchronize()
+        barrier(group)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        e2e_steps = max(1, min(args.steps, 5))
+        for _ in range(e2e_steps):
+            runner.e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        barrier(group)
+        if ops.sync_status() != 0:
+            raise SystemExit("device status not ok in the e2e region")
+        ems = max_over_ranks(a.elapsed_time(b), group)
+        eflops = sum_over_ranks(flops_step * e2e_steps, group)
+        e2e = {"value": eflops / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": runner.h2d_bytes,
+               "d2h_bytes_per_step": runner.d2h_bytes, "ms_per_step": ems / e2e_steps, "steps": e2e_steps,
+               "calls": "linear_fwd / linear_bwd (fused public calls), inputs from pinned host memory"}
+
+    # CPU oracle on a bounded sample (rank 0, single GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = oracle_sample(wl, specs, args.cpu_sample_tokens)
+        t0 = time.perf_counter()
+        f = run_oracle(sample)
+        dt = time.perf_counter() - t0
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": describe_sample(sample) + f" ({dt:.1f} s)", "host_cpus": os.cpu_count()}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
+                "data": "synthetic", "config": workload_config(wl, specs, layers),
+                "roofline": roofline, "roofline_quant": roofline_q, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk, "per_kernel": per_kernel,
+                "gemm_tflop_per_step": flops_step / 1e12, "kernel_source": src_hash}
+        print(json.dumps(line), flush=True)
+    if group is not None:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

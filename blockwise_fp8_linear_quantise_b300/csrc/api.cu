@@ -3,6 +3,7 @@
 // All kernels live in this single translation unit (quant.cuh, gemm.cuh) so
 // the device error word has one definition per loaded module.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -33,6 +34,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_forced_splits = 0;  // 0 = automatic
+std::atomic<uint64_t> g_launches{0};  // kernels launched by this library
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -176,6 +178,7 @@ bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& t
       block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
       break;
   }
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
@@ -186,6 +189,7 @@ bfp8_status launch_quant(const QuantParams& p, bool weight, cudaStream_t st) {
     quantize_tile_kernel<true><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
   else
     quantize_tile_kernel<false><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
@@ -247,6 +251,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   const int rgrid = static_cast<int>(std::min<int64_t>((groups + 7) / 8, int64_t(dev->sms) * 16));
   splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(static_cast<const float*>(ws), g.splits, p.M, p.N,
                                                    static_cast<uint16_t*>(C), Cq, sCq);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
@@ -439,6 +444,8 @@ bfp8_status bfp8_set_gemm_splits(int splits) {
   g_forced_splits = splits;
   return BFP8_OK;
 }
+
+uint64_t bfp8_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* bfp8_status_string(bfp8_status status) {
   switch (status) {

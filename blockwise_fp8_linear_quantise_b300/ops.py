@@ -191,3 +191,8 @@ def set_wait_limit_ns(ns):
 
 def set_gemm_splits(splits):
     _check(_lib.load().bfp8_set_gemm_splits(int(splits)), "set_gemm_splits")
+
+
+def launch_count():
+    """Kernels the library has launched in this process so far."""
+    return int(_lib.load().bfp8_launch_count())

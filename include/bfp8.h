@@ -191,6 +191,13 @@ bfp8_status bfp8_set_wait_limit_ns(uint64_t ns);
  */
 bfp8_status bfp8_set_gemm_splits(int splits);
 
+/*
+ * Number of kernels this library has launched in this process (all devices),
+ * counted on the host at each launch.  A diagnostic for benchmarks that
+ * report how many of the library's kernels ran in a timed region.
+ */
+uint64_t bfp8_launch_count(void);
+
 /* Static description of a status code. */
 const char* bfp8_status_string(bfp8_status status);
 

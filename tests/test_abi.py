@@ -36,6 +36,14 @@ def test_library_exports_every_declared_symbol():
         assert n in _lib.SIGNATURES, f"{n} has no ctypes signature"
 
 
+def test_launch_count_starts_without_gpu_work():
+    # argument errors launch nothing, so the counter does not move
+    lib = _lib.load()
+    before = lib.bfp8_launch_count()
+    assert lib.bfp8_quantize_act_1x128(None, 128, 128, FAKE, FAKE, None, None, None) != 0
+    assert lib.bfp8_launch_count() == before
+
+
 def test_status_strings():
     lib = _lib.load()
     for code in range(7):
