@@ -148,6 +148,50 @@ __device__ __forceinline__ float group_scale(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// Per-group quantisation state.  A code is E4M3_rn_satfinite(fp32_rn(x / s)).
+// Dividing every element is the bulk of the quantisers' instruction count,
+// so codes are taken from y = fp32_rn(x * r) with r = fp32_rn(1 / s) instead,
+// whenever that provably gives the same code:
+//   * s a power of two: r is exact and y = fp32_rn(x / s) exactly;
+//   * otherwise |y - fp32_rn(x / s)| <= 3 * 2^-24 |y| + 2^-148 (two roundings
+//     of r and y plus the quotient's own rounding), so fp32_rn(x / s) lies in
+//     [lo, hi] = [y - d, y + d] (d = 2^-20 |y| + 2^-139, rounded outward).
+//     The E4M3 cast is monotone, so when lo and hi give the same code, so
+//     does every value between them.  Only pairs within about 2^-20 of a
+//     rounding boundary (or at zero) take the IEEE division.
+// The fast path needs a normal, finite s (1/s then stays finite).
+struct GroupScale {
+  float s;     // dequantisation scale amax/448 (1 for an all-zero group)
+  float r;     // fp32_rn(1 / s) when fast
+  bool fast;   // s normal and finite
+  bool exact;  // s a power of two: x * r is the correctly rounded quotient
+};
+
+__device__ __forceinline__ GroupScale make_group_scale(float amax) {
+  GroupScale g;
+  g.s = group_scale(amax);
+  g.fast = g.s >= 0x1p-126f && g.s <= 0x1p+126f;
+  g.r = g.fast ? __frcp_rn(g.s) : 0.0f;
+  g.exact = g.fast && (__float_as_uint(g.s) & 0x007FFFFFu) == 0u;
+  return g;
+}
+
+// Two codes (lo byte = a) of the values a, b under group scale g.
+__device__ __forceinline__ uint32_t quant_pair(float a, float b, const GroupScale& g) {
+  if (g.fast) {
+    const float ya = __fmul_rn(a, g.r), yb = __fmul_rn(b, g.r);
+    if (g.exact) return e4m3x2(ya, yb);
+    const float da = __fmaf_rn(fabsf(ya), 0x1p-20f, 0x1p-139f);
+    const float db = __fmaf_rn(fabsf(yb), 0x1p-20f, 0x1p-139f);
+    // a zero quotient is exact (and keeps its sign); no interval needed
+    const float la = ya == 0.0f ? ya : __fadd_rd(ya, -da), ha = ya == 0.0f ? ya : __fadd_ru(ya, da);
+    const float lb = yb == 0.0f ? yb : __fadd_rd(yb, -db), hb = yb == 0.0f ? yb : __fadd_ru(yb, db);
+    const uint32_t lo = e4m3x2(la, lb);
+    if (lo == static_cast<uint32_t>(e4m3x2(ha, hb))) return lo;
+  }
+  return e4m3x2(__fdiv_rn(a, g.s), __fdiv_rn(b, g.s));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

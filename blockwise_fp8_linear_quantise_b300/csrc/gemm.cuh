@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (p.Cq != nullptr) {
           // E4M3 codes of the bf16 values of this thread's 128-column group,
           // with the activation quantiser's rule (m is their amax).
-          const float s = group_scale(m);
+          const GroupScale g = make_group_scale(m);
           uint8_t* qrow = p.Cq + static_cast<int64_t>(gm) * p.N + col0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -379,12 +379,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c], acc[c + 1]);
               const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
               const uint32_t l = *reinterpret_cast<const uint32_t*>(&lo), h = *reinterpret_cast<const uint32_t*>(&hi);
-              w[j] = static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(l), s), __fdiv_rn(bf16hi(l), s))) |
-                     (static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(h), s), __fdiv_rn(bf16hi(h), s))) << 16);
+              w[j] = quant_pair(bf16lo(l), bf16hi(l), g) | (quant_pair(bf16lo(h), bf16hi(h), g) << 16);
             }
             *reinterpret_cast<uint4*>(qrow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = s;
+          p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = g.s;
           }
         }
       } else {
@@ -430,12 +429,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
     v.y = *reinterpret_cast<const uint32_t*>(&hi);
     *reinterpret_cast<uint2*>(C + off) = v;
     if (Cq != nullptr) {
-      const float s = group_scale(warp_max(fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
-                                                 fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))))));
-      const uint32_t q = e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s)) |
-                         (static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s))) << 16);
+      const GroupScale gs = make_group_scale(warp_max(fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))),
+                                                            fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))))));
+      const uint32_t q = quant_pair(bf16lo(v.x), bf16hi(v.x), gs) | (quant_pair(bf16lo(v.y), bf16hi(v.y), gs) << 16);
       *reinterpret_cast<uint32_t*>(Cq + off) = q;
-      if (lane == 0) sCq[cg * M + r] = s;
+      if (lane == 0) sCq[cg * M + r] = gs.s;
     }
   }
 }

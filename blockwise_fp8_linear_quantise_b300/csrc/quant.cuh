@@ -6,9 +6,11 @@
 // reduction dimension for activations and activation gradients, one per
 // 128x128 block for weights, each computed online from its own values.
 // Per group: amax = max|x| (fmaxf, NaN ignored); s = amax/448 in IEEE fp32
-// (1 when amax == 0); q = E4M3_rn_satfinite(x / s) with an IEEE fp32
-// division.  The codes and scales are therefore fully determined and match a
-// plain CPU evaluation bit for bit.
+// (1 when amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  The codes are
+// taken from x times the rounded reciprocal of s wherever that provably gives
+// the same code, else from the IEEE division (GroupScale / quant_pair), so
+// codes and scales are fully determined and match a plain CPU evaluation bit
+// for bit.
 //
 // Work decomposition: one CTA per 128x128 tile of the bf16 input.  The tile
 // (32 KB) arrives in shared memory by 128 bulk copies of one 256-byte row
@@ -60,16 +62,16 @@ __device__ __forceinline__ void stage_t_row(uint8_t* tileT, int trow, int rq, co
 }
 
 // Quantises the column pair held in w[] (32 rows, low half = column 2cp,
-// high half = column 2cp+1) with scales s0/s1 and stages both code rows.
-__device__ __forceinline__ void quant_column_pair(uint8_t* tileT, int cp, int rq, const uint32_t (&w)[32], float s0,
-                                                  float s1) {
+// high half = column 2cp+1) with group scales g0/g1 and stages both code rows.
+__device__ __forceinline__ void quant_column_pair(uint8_t* tileT, int cp, int rq, const uint32_t (&w)[32],
+                                                  const GroupScale& g0, const GroupScale& g1) {
   uint32_t pk0[8], pk1[8];
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
-    const uint32_t a01 = e4m3x2(__fdiv_rn(bf16lo(w[i]), s0), __fdiv_rn(bf16lo(w[i + 1]), s0));
-    const uint32_t a23 = e4m3x2(__fdiv_rn(bf16lo(w[i + 2]), s0), __fdiv_rn(bf16lo(w[i + 3]), s0));
-    const uint32_t b01 = e4m3x2(__fdiv_rn(bf16hi(w[i]), s1), __fdiv_rn(bf16hi(w[i + 1]), s1));
-    const uint32_t b23 = e4m3x2(__fdiv_rn(bf16hi(w[i + 2]), s1), __fdiv_rn(bf16hi(w[i + 3]), s1));
+    const uint32_t a01 = quant_pair(bf16lo(w[i]), bf16lo(w[i + 1]), g0);
+    const uint32_t a23 = quant_pair(bf16lo(w[i + 2]), bf16lo(w[i + 3]), g0);
+    const uint32_t b01 = quant_pair(bf16hi(w[i]), bf16hi(w[i + 1]), g1);
+    const uint32_t b23 = quant_pair(bf16hi(w[i + 2]), bf16hi(w[i + 3]), g1);
     pk0[i / 4] = a01 | (a23 << 16);
     pk1[i / 4] = b01 | (b23 << 16);
   }
@@ -90,11 +92,9 @@ __device__ __forceinline__ void store_t_tile(const uint8_t* tileT, uint8_t* out,
 }
 
 // Quantises one tile row (128 values) held as 4 values per lane; returns
-// the 4 codes packed.  Scale s is already known.
-__device__ __forceinline__ uint32_t quant4(uint2 v, float s) {
-  const uint32_t lo = e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s));
-  const uint32_t hi = e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s));
-  return lo | (hi << 16);
+// the 4 codes packed.  The group scale is already known.
+__device__ __forceinline__ uint32_t quant4(uint2 v, const GroupScale& g) {
+  return quant_pair(bf16lo(v.x), bf16hi(v.x), g) | (quant_pair(bf16lo(v.y), bf16hi(v.y), g) << 16);
 }
 
 __device__ __forceinline__ float amax4(uint2 v) {
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_tile_kernel(const Quan
   uint8_t* tile = smem;
   uint8_t* tileT = smem + kQTileTOff;
   float* colmax = reinterpret_cast<float*>(smem + kQColMaxOff);
-  float* colscale = reinterpret_cast<float*>(smem + kQColScaleOff);
+  float* colscale = reinterpret_cast<float*>(smem + kQColScaleOff);  // column amax
   float* rowscale = reinterpret_cast<float*>(smem + kQRowScaleOff);
   float* red = reinterpret_cast<float*>(smem + kQRedOff);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kQBarOff);
@@ -138,9 +138,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_tile_kernel(const Quan
     if (p.q != nullptr) {
       for (int rr = warp; rr < 128; rr += kQuantThreads / 32) {
         const uint2 v = *reinterpret_cast<const uint2*>(tile + rr * 256 + lane * 8);
-        const float s = group_scale(warp_max(amax4(v)));
-        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, s);
-        if (lane == 0) rowscale[rr] = s;
+        const GroupScale g = make_group_scale(warp_max(amax4(v)));
+        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, g);
+        if (lane == 0) rowscale[rr] = g.s;
       }
     }
     if (p.qT != nullptr) {
@@ -156,13 +156,13 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_tile_kernel(const Quan
       colmax[rq * 128 + 2 * cp + 1] = m1;
       __syncthreads();
       if (tid < 128) {
+        // colscale holds the column amax; every thread derives the same scale from it
         const float m = fmaxf(fmaxf(colmax[tid], colmax[128 + tid]), fmaxf(colmax[256 + tid], colmax[384 + tid]));
-        const float s = group_scale(m);
-        colscale[tid] = s;
-        p.sT[(r0 / 128) * p.C + c0 + tid] = s;
+        colscale[tid] = m;
+        p.sT[(r0 / 128) * p.C + c0 + tid] = group_scale(m);
       }
       __syncthreads();
-      quant_column_pair(tileT, cp, rq, w, colscale[2 * cp], colscale[2 * cp + 1]);
+      quant_column_pair(tileT, cp, rq, w, make_group_scale(colscale[2 * cp]), make_group_scale(colscale[2 * cp + 1]));
     }
     __syncthreads();
     if (p.q != nullptr && tid < 128) p.s[(c0 / 128) * p.R + r0 + tid] = rowscale[tid];
@@ -181,16 +181,16 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_tile_kernel(const Quan
     float bm = red[0];
 #pragma unroll
     for (int i = 1; i < kQuantThreads / 32; ++i) bm = fmaxf(bm, red[i]);
-    const float s = group_scale(bm);
-    if (tid == 0) p.s[(r0 / 128) * (p.C / 128) + c0 / 128] = s;
+    const GroupScale g = make_group_scale(bm);
+    if (tid == 0) p.s[(r0 / 128) * (p.C / 128) + c0 / 128] = g.s;
     if (p.q != nullptr) {
       for (int rr = warp; rr < 128; rr += kQuantThreads / 32) {
         const uint2 v = *reinterpret_cast<const uint2*>(tile + rr * 256 + lane * 8);
-        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, s);
+        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, g);
       }
     }
     if (p.qT != nullptr) {
-      quant_column_pair(tileT, cp, rq, w, s, s);
+      quant_column_pair(tileT, cp, rq, w, g, g);
       __syncthreads();
       store_t_tile(tileT, p.qT, p.R, c0, r0, tid);
     }

@@ -86,6 +86,31 @@ def test_every_bf16_bit_pattern():
     check_w(xb)
 
 
+@pytest.mark.parametrize("amax", [3.0, 0.7109375, 123.5, 1.0e-30, 5.0e-39, 2.5e38, 3.5, 1.0])
+def test_every_bf16_value_below_a_fixed_amax(amax):
+    """Each 128-group holds +-amax and then every finite bf16 value of smaller
+    magnitude, so x / s sweeps the whole E4M3 range, including values close to
+    its rounding boundaries (non-power-of-two scales), fp32-subnormal scales
+    (amax 5e-39) and power-of-two scales (amax 3.5, 1.0)."""
+    a = np.float32(workloads.to_bf16(np.array([amax], np.float32)).float().numpy()[0])
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = bits[np.isfinite(bits) & (np.abs(bits) <= a)]
+    per = 127
+    groups = -(-vals.size // per)
+    groups += (-groups) % 2                      # an even number of groups -> K = 256 per row
+    padded = np.zeros(groups * per, np.float32)
+    padded[: vals.size] = vals
+    g = padded.reshape(groups, per)
+    first = np.where(np.arange(groups) % 2 == 0, a, -a).astype(np.float32)[:, None]
+    x = np.concatenate([first, g], axis=1).reshape(-1, 256)
+    rows = -(-x.shape[0] // 128) * 128
+    full = np.zeros((rows, 256), np.float32)
+    full[: x.shape[0]] = x
+    xb = workloads.to_bf16(full)
+    check_act(xb)
+    check_w(xb)
+
+
 @pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_gateup", "w"), ("mlp_down", "x"),
                                       ("mlp_down", "w"), ("mlp_down", "dy"), ("attn_proj", "x"),
                                       ("attn_proj", "w_qkv"), ("attn_proj", "dy_qkv")])
