@@ -68,6 +68,11 @@ bfp8_status device_state(DeviceState** out) {
     e = cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
+    // two quantiser CTAs per SM need the largest shared-memory carveout
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
 #define BFP8_SET_GEMM_SMEM(BN, MODE)                                                                     \
   if (e == cudaSuccess)                                                                                   \
     e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
@@ -182,9 +187,14 @@ bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& t
   return cuda_status(cudaGetLastError());
 }
 
+// Persistent quantiser grid: two CTAs per SM (each streams its tiles
+// through a 3-deep shared-memory ring).
 bfp8_status launch_quant(const QuantParams& p, bool weight, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(p.C / 128), static_cast<unsigned>(p.R / 128));
-  if (p.R / 128 > 65535) return BFP8_EUNSUPPORTED;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  const int64_t tiles = (p.R / 128) * (p.C / 128);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
   if (weight)
     quantize_tile_kernel<true><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
   else

@@ -54,14 +54,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One potentially blocking test of the phase with the given parity: the
+// thread may be suspended (up to kSuspendHintNs) until the phase completes,
+// so a waiting warp does not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
+      : "r"(bar_addr), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok;
 }
@@ -133,6 +137,10 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Packed fp32 pair arithmetic (sm_100 family builtins, round to nearest).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 // ------------------------------------------------------------ conversions
 // Two fp32 -> two E4M3 codes (round to nearest even, saturate to +-448);
 // lo lands in the low byte.
@@ -143,53 +151,102 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Scale of a group from its amax: amax/448 (IEEE division), or 1 for amax 0.
+// Scale of a group from its amax: fp32_rn(amax / 448), or 1 for amax 0.
+// amax is the largest magnitude of bf16 values, so it has at most 8
+// significant bits.  For such amax with a normal quotient the quotient is
+// taken as q0 = rn(amax * c), c = rn(1/448), corrected once with the exact
+// residual amax - 448 q0 (Markstein's FMA correction step); checking every
+// positive finite bf16 value against the IEEE quotient shows the result is
+// the correctly rounded one.  Any other input takes the IEEE division.
 __device__ __forceinline__ float group_scale(float amax) {
-  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  if (amax == 0.0f) return 1.0f;
+  const bool bf16_valued = (__float_as_uint(amax) & 0xFFFFu) == 0u;
+  if (bf16_valued && amax >= 448.0f * 0x1p-126f && amax <= 0x1.FEp+127f) {
+    constexpr float c = 1.0f / 448.0f;
+    const float q0 = __fmul_rn(amax, c);
+    const float r = __fmaf_rn(-q0, 448.0f, amax);
+    return __fmaf_rn(r, c, q0);
+  }
+  return __fdiv_rn(amax, 448.0f);
 }
 
 // Per-group quantisation state.  A code is E4M3_rn_satfinite(fp32_rn(x / s)).
-// Dividing every element is the bulk of the quantisers' instruction count,
-// so codes are taken from y = fp32_rn(x * r) with r = fp32_rn(1 / s) instead,
-// whenever that provably gives the same code:
-//   * s a power of two: r is exact and y = fp32_rn(x / s) exactly;
-//   * otherwise |y - fp32_rn(x / s)| <= 3 * 2^-24 |y| + 2^-148 (two roundings
-//     of r and y plus the quotient's own rounding), so fp32_rn(x / s) lies in
-//     [lo, hi] = [y - d, y + d] (d = 2^-20 |y| + 2^-139, rounded outward).
-//     The E4M3 cast is monotone, so when lo and hi give the same code, so
-//     does every value between them.  Only pairs within about 2^-20 of a
-//     rounding boundary (or at zero) take the IEEE division.
-// The fast path needs a normal, finite s (1/s then stays finite).
+// Dividing every element would dominate the quantisers' instruction count,
+// so codes come from two products that bracket the quotient instead:
+//   r ~ 1/s within one ulp (the hardware reciprocal approximation),
+//   ra = rn(r (1 - 2^-19)), rb = rn(r (1 + 2^-19)),  a = rn(x ra), b = rn(x rb).
+// a differs from x/s by the factor (1 - 2^-19) and at most three more
+// relative errors of 2^-24 or 2^-23, so a < (1 - 2^-20) x/s < fp32_rn(x/s)
+// for x > 0, and symmetrically b > fp32_rn(x/s) (mirrored for x < 0).
+// The E4M3 cast is monotone: when a and b give the same code, that is the
+// code of fp32_rn(x/s).  Results below 2^-126 lose relative accuracy but
+// keep the sign of x, and every E4M3 rounding boundary (>= 2^-10) is far
+// above them, so they map to the right signed zero.  When s is a power of
+// two, 1/s is formed exactly from its exponent and x/s is then the
+// correctly rounded product, so ra = rb = 1/s.  Only values within about
+// 2^-19 of a rounding boundary disagree; those take the IEEE division.  A
+// scale whose reciprocal is not a normal number (s subnormal, infinite or
+// NaN) gets ra = 0, rb = inf, which makes every non-NaN value disagree.
 struct GroupScale {
-  float s;     // dequantisation scale amax/448 (1 for an all-zero group)
-  float r;     // fp32_rn(1 / s) when fast
-  bool fast;   // s normal and finite
-  bool exact;  // s a power of two: x * r is the correctly rounded quotient
+  float s;   // dequantisation scale amax/448 (1 for an all-zero group)
+  float ra;  // lower bracketing multiplier
+  float rb;  // upper bracketing multiplier
 };
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ GroupScale make_group_scale(float amax) {
   GroupScale g;
   g.s = group_scale(amax);
-  g.fast = g.s >= 0x1p-126f && g.s <= 0x1p+126f;
-  g.r = g.fast ? __frcp_rn(g.s) : 0.0f;
-  g.exact = g.fast && (__float_as_uint(g.s) & 0x007FFFFFu) == 0u;
+  if (g.s >= 0x1p-126f && g.s <= 0x1p+126f) {
+    const uint32_t sb = __float_as_uint(g.s);
+    if ((sb & 0x007FFFFFu) == 0u) {
+      g.ra = g.rb = __uint_as_float(0x7F000000u - sb);  // exact 1/s for s = 2^k
+    } else {
+      const float r = rcp_approx(g.s);
+      g.ra = __fmul_rn(r, 1.0f - 0x1p-19f);
+      g.rb = __fmul_rn(r, 1.0f + 0x1p-19f);
+    }
+  } else {
+    g.ra = 0.0f;
+    g.rb = __int_as_float(0x7F800000);
+  }
   return g;
 }
 
-// Two codes (lo byte = a) of the values a, b under group scale g.
+// Codes of the pair (x0, x1) (x0 in the low byte) under multipliers ra2/rb2
+// (component k scales x_k).  ORs a nonzero value into `miss` when the two
+// brackets disagree, in which case the returned codes are not to be used.
+__device__ __forceinline__ uint32_t quant_pair_fast(float x0, float x1, float2 ra2, float2 rb2, uint32_t& miss) {
+  const float2 x = make_float2(x0, x1);
+  const float2 a = fmul2(x, ra2), b = fmul2(x, rb2);
+  const uint32_t ca = e4m3x2(a.x, a.y), cb = e4m3x2(b.x, b.y);
+  miss |= ca ^ cb;
+  return ca;
+}
+
+// Reference path: the IEEE quotient, then the cast.
+__device__ __forceinline__ uint32_t quant_pair_div(float x0, float x1, float s0, float s1) {
+  return e4m3x2(__fdiv_rn(x0, s0), __fdiv_rn(x1, s1));
+}
+
+// The division paths are rare.  They live in separate, non-inlined
+// functions behind an unlikely branch, so that the compiler cannot turn
+// them into predicated code that every element would pay for.
+__device__ __noinline__ uint32_t quant_pair_div_call(float x0, float x1, float s) {
+  return quant_pair_div(x0, x1, s, s);
+}
+
+// Two codes (lo byte = a) of the values a, b under one group scale g.
 __device__ __forceinline__ uint32_t quant_pair(float a, float b, const GroupScale& g) {
-  if (g.fast) {
-    const float ya = __fmul_rn(a, g.r), yb = __fmul_rn(b, g.r);
-    if (g.exact) return e4m3x2(ya, yb);
-    const float da = __fmaf_rn(fabsf(ya), 0x1p-20f, 0x1p-139f);
-    const float db = __fmaf_rn(fabsf(yb), 0x1p-20f, 0x1p-139f);
-    // a zero quotient is exact (and keeps its sign); no interval needed
-    const float la = ya == 0.0f ? ya : __fadd_rd(ya, -da), ha = ya == 0.0f ? ya : __fadd_ru(ya, da);
-    const float lb = yb == 0.0f ? yb : __fadd_rd(yb, -db), hb = yb == 0.0f ? yb : __fadd_ru(yb, db);
-    const uint32_t lo = e4m3x2(la, lb);
-    if (lo == static_cast<uint32_t>(e4m3x2(ha, hb))) return lo;
-  }
-  return e4m3x2(__fdiv_rn(a, g.s), __fdiv_rn(b, g.s));
+  uint32_t miss = 0;
+  const uint32_t c = quant_pair_fast(a, b, make_float2(g.ra, g.ra), make_float2(g.rb, g.rb), miss);
+  if (__builtin_expect(miss != 0u, 0)) return quant_pair_div_call(a, b, g.s);
+  return c;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -277,6 +334,13 @@ __device__ __forceinline__ void tmem_wait_ld64(uint32_t* v) {
                  BFP8_W8(56)::"memory");
 }
 
+// Waits for this thread's outstanding tcgen05.ld; ties the 32 registers of
+// the last load to the wait.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t* v) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : BFP8_W8(0), BFP8_W8(8), BFP8_W8(16), BFP8_W8(24)::"memory");
+}
+
 #define BFP8_F8(i) "+f"(a[i]), "+f"(a[i + 1]), "+f"(a[i + 2]), "+f"(a[i + 3]), "+f"(a[i + 4]), "+f"(a[i + 5]), "+f"(a[i + 6]), "+f"(a[i + 7])
 
 // Emits nothing; makes the 64 values a[0..63] final at this point in program
@@ -285,22 +349,8 @@ __device__ __forceinline__ void tmem_wait_ld64(uint32_t* v) {
 __device__ __forceinline__ void reg_fence64(float* a) {
   asm volatile("" : BFP8_F8(0), BFP8_F8(8), BFP8_F8(16), BFP8_F8(24), BFP8_F8(32), BFP8_F8(40), BFP8_F8(48), BFP8_F8(56));
 }
-
-// Packed fp32 pair arithmetic (sm_100 family).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(r)
-      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
-        "l"(*reinterpret_cast<uint64_t*>(&c)));
-  return *reinterpret_cast<float2*>(&r);
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;"
-      : "=l"(r)
-      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
-  return *reinterpret_cast<float2*>(&r);
+__device__ __forceinline__ void reg_fence32(float* a) {
+  asm volatile("" : BFP8_F8(0), BFP8_F8(8), BFP8_F8(16), BFP8_F8(24));
 }
 
 // Register reallocation between warpgroups (all 4 warps of a warpgroup

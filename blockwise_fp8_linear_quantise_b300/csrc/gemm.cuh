@@ -111,6 +111,37 @@ __device__ __forceinline__ UnitCoords unit_coords(const GemmParams& p, int u) {
   return c;
 }
 
+// acc[0..31] += v[0..31] * scale: one scale s2 for the block modes, sa times
+// the 32 per-column scales at sbc for kSbCol.
+template <int SBMODE>
+__device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], float2 s2, float2 sa2,
+                                          const float* sbc) {
+  if constexpr (SBMODE != kSbCol) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 a2 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), s2,
+                              make_float2(acc[i], acc[i + 1]));
+      acc[i] = a2.x;
+      acc[i + 1] = a2.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 sb4 = *reinterpret_cast<const float4*>(sbc + i);
+      const float2 sc0 = fmul2(sa2, make_float2(sb4.x, sb4.y));
+      const float2 sc1 = fmul2(sa2, make_float2(sb4.z, sb4.w));
+      const float2 a0 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc0,
+                              make_float2(acc[i], acc[i + 1]));
+      const float2 a1 = ffma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), sc1,
+                              make_float2(acc[i + 2], acc[i + 3]));
+      acc[i] = a0.x;
+      acc[i + 1] = a0.y;
+      acc[i + 2] = a1.x;
+      acc[i + 3] = a1.y;
+    }
+  }
+}
+
 template <int BN, int SBMODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -290,53 +321,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + b * BN + half * kCols;
-        if constexpr (SBMODE != kSbCol) {
-          const float s = sa_cur * sb_cur;
-          const float2 s2 = make_float2(s, s);
+        // acc[j] += P[j] * scale(j) over this thread's kCols columns, read from
+        // TMEM in 32-column chunks: the load of chunk c+1 is in flight while
+        // chunk c is multiplied in.  The buffer is released as soon as its
+        // last chunk is in registers.
+        const float s = sa_cur * sb_cur;
+        const float2 s2 = make_float2(s, s);
+        const float2 sa2 = make_float2(sa_cur, sa_cur);
+        const float* sbc = ring + b * BN + half * kCols;
+        uint32_t va[32], vb[32];
+        tmem_ld32(taddr, va);
+        tmem_wait_ld32(va);
 #pragma unroll
-          for (int r = 0; r < kCols / 64; ++r) {
-            uint32_t v[64];
-            tmem_ld32(taddr + r * 64, v);
-            tmem_ld32(taddr + r * 64 + 32, v + 32);
-            tmem_wait_ld64(v);
-#pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-              float2 a2 = make_float2(acc[r * 64 + i], acc[r * 64 + i + 1]);
-              a2 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), s2, a2);
-              acc[r * 64 + i] = a2.x;
-              acc[r * 64 + i + 1] = a2.y;
-            }
-            reg_fence64(acc + r * 64);
+        for (int ch = 0; ch < kCols / 32; ch += 2) {
+          tmem_ld32(taddr + (ch + 1) * 32, vb);
+          promote32<SBMODE>(acc + ch * 32, va, s2, sa2, sbc + ch * 32);
+          reg_fence32(acc + ch * 32);
+          tmem_wait_ld32(vb);
+          if (ch + 2 < kCols / 32) {
+            tmem_ld32(taddr + (ch + 2) * 32, va);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
           }
-        } else {
-          const float* sbc = ring + b * BN + half * kCols;
-          const float2 sa2 = make_float2(sa_cur, sa_cur);
-#pragma unroll
-          for (int r = 0; r < kCols / 64; ++r) {
-            uint32_t v[64];
-            tmem_ld32(taddr + r * 64, v);
-            tmem_ld32(taddr + r * 64 + 32, v + 32);
-            tmem_wait_ld64(v);
-#pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-              const float4 sb4 = *reinterpret_cast<const float4*>(sbc + r * 64 + i);
-              const float2 sc0 = fmul2(sa2, make_float2(sb4.x, sb4.y));
-              const float2 sc1 = fmul2(sa2, make_float2(sb4.z, sb4.w));
-              float2 a0 = make_float2(acc[r * 64 + i], acc[r * 64 + i + 1]);
-              float2 a1 = make_float2(acc[r * 64 + i + 2], acc[r * 64 + i + 3]);
-              a0 = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc0, a0);
-              a1 = ffma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), sc1, a1);
-              acc[r * 64 + i] = a0.x;
-              acc[r * 64 + i + 1] = a0.y;
-              acc[r * 64 + i + 2] = a1.x;
-              acc[r * 64 + i + 3] = a1.y;
-            }
-            reg_fence64(acc + r * 64);
-          }
+          promote32<SBMODE>(acc + (ch + 1) * 32, vb, s2, sa2, sbc + (ch + 1) * 32);
+          reg_fence32(acc + (ch + 1) * 32);
+          if (ch + 2 < kCols / 32) tmem_wait_ld32(va);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
         if constexpr (SBMODE == kSbCol) {
           // Everyone has passed this slice's ring wait, so every thread is
           // done with slot (it+1)&1 (last read for slice it-1): refill it.

@@ -5,25 +5,32 @@
 // $5090", section 3.2: one scale per 128 consecutive values along the GEMM
 // reduction dimension for activations and activation gradients, one per
 // 128x128 block for weights, each computed online from its own values.
-// Per group: amax = max|x| (fmaxf, NaN ignored); s = amax/448 in IEEE fp32
-// (1 when amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  The codes are
-// taken from x times the rounded reciprocal of s wherever that provably gives
-// the same code, else from the IEEE division (GroupScale / quant_pair), so
-// codes and scales are fully determined and match a plain CPU evaluation bit
-// for bit.
+// Per group: amax = max|x| (NaN ignored); s = amax/448 in IEEE fp32 (1 when
+// amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  Codes come from the
+// bracketing products of GroupScale wherever those provably agree and from
+// the IEEE division otherwise, so codes and scales match a plain CPU
+// evaluation bit for bit.
 //
-// Work decomposition: one CTA per 128x128 tile of the bf16 input.  The tile
-// (32 KB) arrives in shared memory by 128 bulk copies of one 256-byte row
-// each; the CTA then
-//   * row pass:    each warp takes whole tile rows; a lane holds 4 values,
-//                  a 5-step shuffle gives the row-group amax; codes leave as
-//                  one coalesced 128-byte store per row;
-//   * column pass: each thread holds a column pair over 32 rows in registers;
-//                  4 partial amaxes per column meet in shared memory; the
-//                  transposed codes are staged in a swizzled [128][128] byte
-//                  tile and leave as coalesced 16-byte stores.
-// The input is read from HBM once whichever outputs are requested, so the
-// dual quantiser moves 2 B in + 2 B out (+ scales) per element.
+// Work decomposition.  The input is cut into 128x128 bf16 tiles (32 KB),
+// walked in row-major order by a persistent grid (two CTAs per SM).  A CTA
+// streams its tiles through a 3-deep shared-memory ring filled by bulk
+// copies; its eight warps share each tile without any block-wide barrier
+// (warp 0 also refills a slot once every warp has released it).  Warp w owns
+//   * rows 16w..16w+15 (their 1x128 groups along the columns: q, s): lane
+//     pair (2j, 2j+1) holds row 16w+j, 64 values each, as the 16-code output
+//     chunks 2m+h (h = lane & 1), and
+//   * columns 16w..16w+15 (their groups of 128 rows: qT, sT): lane l holds
+//     columns 16w+4(l%4)..+3 over rows 16(l/4)..16(l/4)+15.
+// It copies both slices into registers, releases the ring slot, reduces
+// amaxes with in-lane packed bf16 maxima and a few shuffles, turns each
+// amax into its scale once per warp instruction stream, and stores codes
+// straight to global memory in 32-byte (rows) and 128-byte (columns)
+// segments.  The input is read from HBM once whichever outputs are requested.
+//
+// Shared-memory image of a tile: row r (256 bytes) starts at byte
+// 272 r + 16 ((r / 16) % 8).  The 16-byte stride padding and the per-block
+// offset make both register views conflict-free: 16 consecutive rows fall on
+// all eight 16-byte bank groups twice, and rows 16 apart on distinct ones.
 #pragma once
 
 #include "common.cuh"
@@ -40,160 +47,255 @@ struct QuantParams {
   uint64_t wait_ns;
 };
 
-constexpr int kQuantThreads = 256;
-constexpr int kQTileBytes = 128 * 256;                       // bf16 tile
-constexpr int kQTileTOff = kQTileBytes;                      // [128][128] codes
-constexpr int kQColMaxOff = kQTileTOff + 128 * 128;          // float[4][128]
-constexpr int kQColScaleOff = kQColMaxOff + 4 * 128 * 4;     // float[128]
-constexpr int kQRowScaleOff = kQColScaleOff + 128 * 4;       // float[128]
-constexpr int kQRedOff = kQRowScaleOff + 128 * 4;            // float[8]
-constexpr int kQBarOff = kQRedOff + 8 * 4;                   // uint64
-constexpr int kQuantSmemBytes = kQBarOff + 16;
+constexpr int kQComputeWarps = 8;
+constexpr int kQuantThreads = 32 * kQComputeWarps;
+constexpr int kQStages = 3;
+constexpr int kQTileBytes = 128 * 256;                     // bf16 payload of a tile
+constexpr int kQBufBytes = 34944;                          // padded image, >= 272*127 + 16*7 + 256
+constexpr int kQBarOff = kQStages * kQBufBytes;            // full[3], empty[3], redbar[2]
+constexpr int kQRedOff = kQBarOff + (2 * kQStages + 2) * 8;  // float[2][8] (weight block amax)
+constexpr int kQuantSmemBytes = kQRedOff + 2 * kQComputeWarps * 4;
+static_assert(272 * 127 + 16 * 7 + 256 <= kQBufBytes, "tile image overflows its buffer");
 
-// Writes the 32 codes of one column (32 consecutive rows of the tile) into
-// row `trow` of the transposed staging tile.  16-byte chunk c of a staging
-// row is stored at chunk c ^ ((trow >> 1) & 7), which keeps both the writes
-// here (8 lanes -> 8 rows 2 apart) and the row-wise reads conflict-free.
-__device__ __forceinline__ void stage_t_row(uint8_t* tileT, int trow, int rq, const uint32_t (&pk)[8]) {
-  const int sw = (trow >> 1) & 7;
-  uint8_t* row = tileT + trow * 128;
-  *reinterpret_cast<uint4*>(row + (((2 * rq) ^ sw) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  *reinterpret_cast<uint4*>(row + (((2 * rq + 1) ^ sw) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+__device__ __forceinline__ uint32_t qrow_off(int r) { return 272u * r + 16u * ((r >> 4) & 7); }
+
+__device__ __forceinline__ float bf16x2_absmax(uint32_t w) { return fmaxf(fabsf(bf16lo(w)), fabsf(bf16hi(w))); }
+
+// max(|a|, |b|) per bf16 half (NaN ignored); the sign bits of the result are
+// meaningless and are dropped when the halves are widened.
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// Quantises the column pair held in w[] (32 rows, low half = column 2cp,
-// high half = column 2cp+1) with group scales g0/g1 and stages both code rows.
-__device__ __forceinline__ void quant_column_pair(uint8_t* tileT, int cp, int rq, const uint32_t (&w)[32],
-                                                  const GroupScale& g0, const GroupScale& g1) {
-  uint32_t pk0[8], pk1[8];
+// 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i) by
+// the IEEE division: the rare path of quant16 / quant_col16 (not inlined,
+// so that its divisions are never predicated into the common path).
+__device__ __noinline__ uint4 quant16_div(uint4 a, uint4 b, float s) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[8];
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    const uint32_t a01 = quant_pair(bf16lo(w[i]), bf16lo(w[i + 1]), g0);
-    const uint32_t a23 = quant_pair(bf16lo(w[i + 2]), bf16lo(w[i + 3]), g0);
-    const uint32_t b01 = quant_pair(bf16hi(w[i]), bf16hi(w[i + 1]), g1);
-    const uint32_t b23 = quant_pair(bf16hi(w[i + 2]), bf16hi(w[i + 3]), g1);
-    pk0[i / 4] = a01 | (a23 << 16);
-    pk1[i / 4] = b01 | (b23 << 16);
-  }
-  stage_t_row(tileT, 2 * cp, rq, pk0);
-  stage_t_row(tileT, 2 * cp + 1, rq, pk1);
+  for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), s, s);
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
-// Copies the staged transposed codes to out[(c0 + row) * ld + r0 + ...].
-__device__ __forceinline__ void store_t_tile(const uint8_t* tileT, uint8_t* out, int64_t ld, int64_t c0, int64_t r0,
-                                             int tid) {
+// 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
+__device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
+  const float2 ra = make_float2(g.ra, g.ra), rb = make_float2(g.rb, g.rb);
+  uint32_t miss = 0;
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int idx = tid + kQuantThreads * j;
-    const int row = idx >> 3, ch = idx & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(tileT + row * 128 + ((ch ^ ((row >> 1) & 7)) << 4));
-    *reinterpret_cast<uint4*>(out + (c0 + row) * ld + r0 + ch * 16) = v;
+  for (int i = 0; i < 8; ++i) c[i] = quant_pair_fast(bf16lo(w[i]), bf16hi(w[i]), ra, rb, miss);
+  if (__builtin_expect(miss != 0u, 0)) return quant16_div(a, b, g.s);
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+}
+
+// Values k and k+1 of one column (element kHalf of word kWord of row slices
+// k and k+1 in v[]) packed as one bf16 pair, row k in the low half.
+template <int kWord, int kHalf>
+__device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
+  const uint32_t w0 = kWord ? v[k].y : v[k].x, w1 = kWord ? v[k + 1].y : v[k + 1].x;
+  return kHalf ? __byte_perm(w0, w1, 0x7632) : __byte_perm(w0, w1, 0x5410);
+}
+
+// 16 codes of one column over 16 rows, one group.  Codes in row order.
+template <int kWord, int kHalf>
+__device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], float ra_, float rb_, float s) {
+  const float2 ra = make_float2(ra_, ra_), rb = make_float2(rb_, rb_);
+  uint32_t miss = 0, c[8];
+#pragma unroll
+  for (int k = 0; k < 16; k += 2) {
+    const uint32_t w0 = kWord ? v[k].y : v[k].x, w1 = kWord ? v[k + 1].y : v[k + 1].x;
+    c[k / 2] = quant_pair_fast(kHalf ? bf16hi(w0) : bf16lo(w0), kHalf ? bf16hi(w1) : bf16lo(w1), ra, rb, miss);
   }
+  if (__builtin_expect(miss != 0u, 0)) {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
+    return quant16_div(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]), s);
+  }
+  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
-// Quantises one tile row (128 values) held as 4 values per lane; returns
-// the 4 codes packed.  The group scale is already known.
-__device__ __forceinline__ uint32_t quant4(uint2 v, const GroupScale& g) {
-  return quant_pair(bf16lo(v.x), bf16hi(v.x), g) | (quant_pair(bf16lo(v.y), bf16hi(v.y), g) << 16);
-}
-
-__device__ __forceinline__ float amax4(uint2 v) {
-  return fmaxf(fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x))), fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))));
+// kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
+// kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
+// Issues the bulk copies of tile t into ring slot `buf` (one whole warp;
+// lane 0 arms the slot's barrier).
+__device__ __forceinline__ void quant_fill(const QuantParams& p, int64_t t, int64_t ctiles, uint8_t* buf,
+                                           uint64_t* bar, int lane) {
+  const int64_t r0 = (t / ctiles) * 128, c0 = (t % ctiles) * 128;
+  if (lane == 0) mbar_arrive_expect_tx(bar, kQTileBytes);
+  __syncwarp();
+  for (int r = lane; r < 128; r += 32) bulk_g2s(buf + qrow_off(r), p.x + (r0 + r) * p.C + c0, 256, bar);
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
 // kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
 template <bool kWeight>
-__global__ void __launch_bounds__(kQuantThreads) quantize_tile_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const QuantParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* tile = smem;
-  uint8_t* tileT = smem + kQTileTOff;
-  float* colmax = reinterpret_cast<float*>(smem + kQColMaxOff);
-  float* colscale = reinterpret_cast<float*>(smem + kQColScaleOff);  // column amax
-  float* rowscale = reinterpret_cast<float*>(smem + kQRowScaleOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQBarOff);
+  uint64_t* empty = full + kQStages;
+  uint64_t* redbar = empty + kQStages;  // weight block amax exchange, by tile parity
   float* red = reinterpret_cast<float*>(smem + kQRedOff);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kQBarOff);
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ctiles = p.C / 128;
+  const int64_t tiles = (p.R / 128) * ctiles;
 
-  if (tid == 0) {
-    mbar_init(bar, 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kQComputeWarps);
+    }
+    mbar_init(&redbar[0], kQComputeWarps);
+    mbar_init(&redbar[1], kQComputeWarps);
     fence_mbar_init();
   }
   __syncthreads();
+  // prologue: the first kQStages tiles of this CTA
+  uint32_t issued = 0;  // tiles whose copies warp 0 has issued
   if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, kQTileBytes);
-    __syncwarp();
-    for (int i = lane; i < 128; i += 32) bulk_g2s(tile + i * 256, p.x + (r0 + i) * p.C + c0, 256, bar);
+    int64_t t = blockIdx.x;
+    for (int s = 0; s < kQStages && t < tiles; ++s, t += gridDim.x, ++issued)
+      quant_fill(p, t, ctiles, smem + s * kQBufBytes, &full[s], lane);
   }
-  const bool ok = mbar_wait(bar, 0, p.wait_ns, kWeight ? 0x201u : 0x101u);
-  if (__syncthreads_or(!ok)) return;
 
-  const uint32_t* t32 = reinterpret_cast<const uint32_t*>(tile);
-  const int cp = tid & 63, rq = tid >> 6;
+  const bool rows = p.q != nullptr, cols = p.qT != nullptr;
+  const int rj = lane >> 1, rh = lane & 1;   // row view: row 16w + rj, chunks 2m + rh
+  const int cq = lane & 3, rg = lane >> 2;   // column view: columns 16w + 4cq.., rows 16rg..
+  const int wrow = 16 * warp + rj;
+  uint32_t j = 0;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+    const uint32_t s = j % kQStages, ph = (j / kQStages) & 1u;
+    if (!mbar_wait(&full[s], ph, p.wait_ns, kWeight ? 0x201u : 0x101u)) break;
+    const uint8_t* buf = smem + s * kQBufBytes;
+    const int64_t r0 = (t / ctiles) * 128, c0 = (t % ctiles) * 128;
 
-  if constexpr (!kWeight) {
-    if (p.q != nullptr) {
-      for (int rr = warp; rr < 128; rr += kQuantThreads / 32) {
-        const uint2 v = *reinterpret_cast<const uint2*>(tile + rr * 256 + lane * 8);
-        const GroupScale g = make_group_scale(warp_max(amax4(v)));
-        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, g);
-        if (lane == 0) rowscale[rr] = g.s;
-      }
-    }
-    if (p.qT != nullptr) {
-      uint32_t w[32];
-      float m0 = 0.0f, m1 = 0.0f;
+    // both slices into registers, then hand the slot back
+    uint4 rv[8];
+    uint2 cv[16];
+    if (rows) {
+      const uint8_t* rp = buf + qrow_off(wrow);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        w[i] = t32[(rq * 32 + i) * 64 + cp];
-        m0 = fmaxf(m0, fabsf(bf16lo(w[i])));
-        m1 = fmaxf(m1, fabsf(bf16hi(w[i])));
+      for (int m = 0; m < 4; ++m) {
+        rv[2 * m] = *reinterpret_cast<const uint4*>(rp + (2 * (2 * m + rh)) * 16);
+        rv[2 * m + 1] = *reinterpret_cast<const uint4*>(rp + (2 * (2 * m + rh) + 1) * 16);
       }
-      colmax[rq * 128 + 2 * cp] = m0;
-      colmax[rq * 128 + 2 * cp + 1] = m1;
-      __syncthreads();
-      if (tid < 128) {
-        // colscale holds the column amax; every thread derives the same scale from it
-        const float m = fmaxf(fmaxf(colmax[tid], colmax[128 + tid]), fmaxf(colmax[256 + tid], colmax[384 + tid]));
-        colscale[tid] = m;
-        p.sT[(r0 / 128) * p.C + c0 + tid] = group_scale(m);
-      }
-      __syncthreads();
-      quant_column_pair(tileT, cp, rq, w, make_group_scale(colscale[2 * cp]), make_group_scale(colscale[2 * cp + 1]));
     }
-    __syncthreads();
-    if (p.q != nullptr && tid < 128) p.s[(c0 / 128) * p.R + r0 + tid] = rowscale[tid];
-    if (p.qT != nullptr) store_t_tile(tileT, p.qT, p.R, c0, r0, tid);
-  } else {
-    uint32_t w[32];
-    float m = 0.0f;
+    if (cols) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      w[i] = t32[(rq * 32 + i) * 64 + cp];
-      m = fmaxf(m, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+      for (int k = 0; k < 16; ++k)
+        cv[k] = *reinterpret_cast<const uint2*>(buf + qrow_off(16 * rg + k) + 32 * warp + 8 * cq);
     }
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    float bm = red[0];
-#pragma unroll
-    for (int i = 1; i < kQuantThreads / 32; ++i) bm = fmaxf(bm, red[i]);
-    const GroupScale g = make_group_scale(bm);
-    if (tid == 0) p.s[(r0 / 128) * (p.C / 128) + c0 / 128] = g.s;
-    if (p.q != nullptr) {
-      for (int rr = warp; rr < 128; rr += kQuantThreads / 32) {
-        const uint2 v = *reinterpret_cast<const uint2*>(tile + rr * 256 + lane * 8);
-        *reinterpret_cast<uint32_t*>(p.q + (r0 + rr) * p.C + c0 + lane * 4) = quant4(v, g);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (warp == 0) {
+      // refill the slot of tile j-1 (every warp released it, usually long
+      // ago) with tile j-1+kQStages
+      const int64_t tn = t + (kQStages - 1) * static_cast<int64_t>(gridDim.x);
+      if (j >= 1 && tn < tiles) {
+        const uint32_t f = j - 1, sf = f % kQStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        quant_fill(p, tn, ctiles, smem + sf * kQBufBytes, &full[sf], lane);
+        ++issued;
       }
     }
-    if (p.qT != nullptr) {
-      quant_column_pair(tileT, cp, rq, w, g, g);
-      __syncthreads();
-      store_t_tile(tileT, p.qT, p.R, c0, r0, tid);
+
+    // amaxes (packed bf16, NaN ignored)
+    float row_m = 0.0f;
+    uint32_t m01 = 0u, m23 = 0u;
+    if (rows) {
+      uint32_t m2 = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        m2 = bf16x2_maxabs(bf16x2_maxabs(m2, bf16x2_maxabs(rv[k].x, rv[k].y)), bf16x2_maxabs(rv[k].z, rv[k].w));
+      row_m = bf16x2_absmax(m2);
+      row_m = fmaxf(row_m, __shfl_xor_sync(0xffffffffu, row_m, 1));
     }
+    if (cols) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        m01 = bf16x2_maxabs(m01, cv[k].x);
+        m23 = bf16x2_maxabs(m23, cv[k].y);
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        m01 = bf16x2_maxabs(m01, __shfl_xor_sync(0xffffffffu, m01, o));
+        m23 = bf16x2_maxabs(m23, __shfl_xor_sync(0xffffffffu, m23, o));
+      }
+    }
+
+    GroupScale grow, gcol;  // this lane's row group; column 4cq + rg%4 (scales of the other columns by shuffle)
+    if constexpr (kWeight) {
+      // one block: every warp's maxima meet in shared memory.  Slot j%2 is
+      // reused two tiles later, when every warp has read it (a warp arrives
+      // for tile j+1 only after reading slot j%2).
+      float m = rows ? row_m : fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23));
+      m = warp_max(m);
+      float* rbuf = red + (j & 1u) * kQComputeWarps;
+      if (lane == 0) {
+        rbuf[warp] = m;
+        mbar_arrive(&redbar[j & 1u]);
+      }
+      if (!mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, p.wait_ns, 0x221u)) break;
+      float bm = rbuf[0];
+#pragma unroll
+      for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
+      grow = make_group_scale(bm);
+      gcol = grow;
+      if (threadIdx.x == 0) p.s[(r0 / 128) * (p.C / 128) + c0 / 128] = grow.s;
+    } else {
+      if (rows) {
+        grow = make_group_scale(row_m);
+        if (rh == 0) p.s[(c0 / 128) * p.R + r0 + wrow] = grow.s;
+      }
+      if (cols) {
+        const int sel = rg & 3;
+        const uint32_t mw = sel < 2 ? m01 : m23;
+        gcol = make_group_scale(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
+        if (rg < 4) p.sT[(r0 / 128) * p.C + c0 + 16 * warp + 4 * cq + rg] = gcol.s;
+      }
+    }
+
+    // codes
+    if (rows) {
+      uint8_t* qrow = p.q + (r0 + wrow) * p.C + c0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(qrow + (2 * m + rh) * 16) = quant16(rv[2 * m], rv[2 * m + 1], grow);
+    }
+    if (cols) {
+      // the scales of this lane's 4 columns live in lanes cq + 4k
+      float ra[4], rb[4], sc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if constexpr (kWeight) {
+          ra[k] = gcol.ra;
+          rb[k] = gcol.rb;
+          sc[k] = gcol.s;
+        } else {
+          ra[k] = __shfl_sync(0xffffffffu, gcol.ra, cq + 4 * k);
+          rb[k] = __shfl_sync(0xffffffffu, gcol.rb, cq + 4 * k);
+          sc[k] = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
+        }
+      }
+      uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
+      *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0>(cv, ra[0], rb[0], sc[0]);
+      *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1>(cv, ra[1], rb[1], sc[1]);
+      *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0>(cv, ra[2], rb[2], sc[2]);
+      *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1>(cv, ra[3], rb[3], sc[3]);
+    }
+  }
+  // Leave no copy in flight into this CTA's shared memory: after an early
+  // exit, wait (bounded) for the tiles issued but not consumed.
+  if (warp == 0 && lane == 0) {
+    for (uint32_t k = j; k < issued; ++k)
+      mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, p.wait_ns, kWeight ? 0x212u : 0x112u);
   }
 }
 

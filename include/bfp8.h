@@ -131,6 +131,7 @@ bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout,
 /* Scratch bytes bfp8_fp8_block_gemm needs for these arguments (0 when none). */
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K);
 
+
 /*
  * Fused forward of one linear layer, Y [M, N] = X [M, K] . W [N, K]^T
  * (section 3.2: W stays bf16/fp32 and is re-quantised on every use; FP8 is

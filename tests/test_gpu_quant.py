@@ -111,6 +111,27 @@ def test_every_bf16_value_below_a_fixed_amax(amax):
     check_w(xb)
 
 
+def test_every_bf16_value_as_group_amax():
+    """Row group g (128 values along K) has amax = the g-th positive finite
+    bf16 value, so every scale amax/448 reachable from bf16 inputs is formed
+    once (normal and subnormal quotients alike); the other 127 values of the
+    group are that amax times uniform(-1, 1), rounded to bf16."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint32) << 16
+    amax = bits.view(np.float32)
+    rng = np.random.default_rng(7)
+    groups = np.empty((amax.size, 128), np.float32)
+    groups[:, 0] = np.where(rng.random(amax.size) < 0.5, amax, -amax)
+    groups[:, 1:] = amax[:, None] * rng.uniform(-1, 1, (amax.size, 127)).astype(np.float32)
+    xb = workloads.to_bf16(groups)
+    # rounding to bf16 can reach the amax but not exceed it
+    assert np.all(np.abs(xb.float().numpy()).max(axis=1) == amax)
+    n = -(-amax.size // 256) * 256
+    full = np.zeros((n, 128), np.float32)
+    full[: amax.size] = xb.float().numpy()
+    x = workloads.to_bf16(full.reshape(-1, 256))
+    check_act(x)
+
+
 @pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_gateup", "w"), ("mlp_down", "x"),
                                       ("mlp_down", "w"), ("mlp_down", "dy"), ("attn_proj", "x"),
                                       ("attn_proj", "w_qkv"), ("attn_proj", "dy_qkv")])
