@@ -346,6 +346,58 @@ int current_sms() {
 
 }  // namespace
 
+// ----------------------------------------------------------------------------
+// GEMM entry point that allocates nothing: its split-K scratch is a static
+// device array of this module.  The array's name in host code is only a
+// host-side stand-in, so its device address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and passed
+// to the kernels like any other workspace pointer.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BFP8_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call per device).
+bfp8_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BFP8_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BFP8_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return BFP8_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return BFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bfp8_status bfp8_fp8_block_gemm_noalloc(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B,
+                                        const float* sb, int64_t M, int64_t N, int64_t K, void* C, uint8_t* Cq,
+                                        float* sCq, bfp8_stream_t stream) {
+  if (layout != BFP8_FPROP && layout != BFP8_DGRAD && layout != BFP8_WGRAD) return BFP8_EINVAL;
+  if (!A || !sa || !B || !sb || !C || (Cq == nullptr) != (sCq == nullptr)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != BFP8_OK) return s;
+  // The split-K partials of these sizes must fit in the static array.
+  if (plan_gemm(M, N, K, dev->sms).ws_bytes > static_cast<size_t>(BFP8_NOALLOC_SCRATCH_BYTES)) return BFP8_EWORKSPACE;
+  return gemm_impl(layout, A, sa, B, sb, M, N, K, C, Cq, sCq, scratch, BFP8_NOALLOC_SCRATCH_BYTES,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
 extern "C" {
 
 bfp8_status bfp8_quantize_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,

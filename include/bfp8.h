@@ -131,6 +131,40 @@ bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout,
 /* Scratch bytes bfp8_fp8_block_gemm needs for these arguments (0 when none). */
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K);
 
+/*
+ * The same GEMM as bfp8_fp8_block_gemm, for callers that cannot allocate
+ * device memory: code that runs where cudaMalloc is not allowed or not
+ * wanted (inside a host callback, a custom allocator, a real-time loop
+ * that must not synchronise the device), or that has no way to hand over a
+ * workspace.  The paper has no counterpart; this is a convenience of the
+ * library.
+ *
+ * Arguments, layouts and results are those of bfp8_fp8_block_gemm without
+ * the workspace: the caller still passes every input and output.  The
+ * split-K partial sums go to one static device array of
+ * BFP8_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  This entry point calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one array.  Calls that run at the same time on
+ *     the GPU (different streams or threads) race on it and corrupt each
+ *     other's results: serialise them.  Each call overwrites every partial
+ *     it reads, so nothing has to be cleared between calls.
+ *   - Sizes whose split-K partials (splits x M x N x 4 bytes, with the split
+ *     count bfp8_fp8_block_gemm would use) exceed the array are rejected
+ *     with BFP8_EWORKSPACE before anything is launched.
+ * Errors: EINVAL, EALIGN, EWORKSPACE, EUNSUPPORTED, ECUDA.
+ */
+#define BFP8_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+bfp8_status bfp8_fp8_block_gemm_noalloc(bfp8_layout layout,
+                                        const uint8_t* A, const float* sa,
+                                        const uint8_t* B, const float* sb,
+                                        int64_t M, int64_t N, int64_t K,
+                                        void* C, uint8_t* Cq, float* sCq,
+                                        bfp8_stream_t stream);
 
 /*
  * Fused forward of one linear layer, Y [M, N] = X [M, K] . W [N, K]^T
