@@ -171,62 +171,58 @@ __device__ __forceinline__ float group_scale(float amax) {
 }
 
 // Per-group quantisation state.  A code is E4M3_rn_satfinite(fp32_rn(x / s)).
-// Dividing every element would dominate the quantisers' instruction count,
-// so codes come from two products that bracket the quotient instead:
-//   r ~ 1/s within one ulp (the hardware reciprocal approximation),
-//   ra = rn(r (1 - 2^-19)), rb = rn(r (1 + 2^-19)),  a = rn(x ra), b = rn(x rb).
-// a differs from x/s by the factor (1 - 2^-19) and at most three more
-// relative errors of 2^-24 or 2^-23, so a < (1 - 2^-20) x/s < fp32_rn(x/s)
-// for x > 0, and symmetrically b > fp32_rn(x/s) (mirrored for x < 0).
-// The E4M3 cast is monotone: when a and b give the same code, that is the
-// code of fp32_rn(x/s).  Results below 2^-126 lose relative accuracy but
-// keep the sign of x, and every E4M3 rounding boundary (>= 2^-10) is far
-// above them, so they map to the right signed zero.  When s is a power of
-// two, 1/s is formed exactly from its exponent and x/s is then the
-// correctly rounded product, so ra = rb = 1/s.  Only values within about
-// 2^-19 of a rounding boundary disagree; those take the IEEE division.  A
-// scale whose reciprocal is not a normal number (s subnormal, infinite or
-// NaN) gets ra = 0, rb = inf, which makes every non-NaN value disagree.
+// A division per element would dominate the quantisers' instruction count,
+// so the correctly rounded quotient Q = fp32_rn(x / s) is formed with
+// Markstein's FMA correction (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev., 1990;
+// as stated in Muller et al., Handbook of Floating-Point Arithmetic):
+//   r = RN(1/s)                      once per group (IEEE reciprocal);
+//   y = RN(x r)                      within 1.5 ulp of x/s;
+//   y = RN(y + r RN(x - s y))        one refinement: now within one ulp;
+//   Q = RN(y + r (x - s y))          x - s y is exact (FMA remainder of a
+//                                    faithful quotient), and with r = RN(1/s)
+//                                    the theorem gives Q = RN(x/s) (up to
+//                                    the sign of a zero, restored from x).
+// No step overflows or loses the remainder to underflow while s lies in
+// [2^-80, 2^100]: every quotient that can reach an E4M3 code (|x/s| >=
+// 2^-11) then has a remainder at or above 2^-137, and smaller quotients keep
+// the sign of x and stay far below the smallest E4M3 rounding boundary
+// (2^-10), so they still map to the right signed zero.  A group whose scale
+// lies outside that range (or is not finite) takes the IEEE division.
 struct GroupScale {
-  float s;   // dequantisation scale amax/448 (1 for an all-zero group)
-  float ra;  // lower bracketing multiplier
-  float rb;  // upper bracketing multiplier
+  float s;     // dequantisation scale amax/448 (1 for an all-zero group)
+  float r;     // RN(1/s)
+  bool exact;  // s within [2^-80, 2^100]: the FMA path applies
 };
-
-__device__ __forceinline__ float rcp_approx(float x) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
 
 __device__ __forceinline__ GroupScale make_group_scale(float amax) {
   GroupScale g;
   g.s = group_scale(amax);
-  if (g.s >= 0x1p-126f && g.s <= 0x1p+126f) {
-    const uint32_t sb = __float_as_uint(g.s);
-    if ((sb & 0x007FFFFFu) == 0u) {
-      g.ra = g.rb = __uint_as_float(0x7F000000u - sb);  // exact 1/s for s = 2^k
-    } else {
-      const float r = rcp_approx(g.s);
-      g.ra = __fmul_rn(r, 1.0f - 0x1p-19f);
-      g.rb = __fmul_rn(r, 1.0f + 0x1p-19f);
-    }
-  } else {
-    g.ra = 0.0f;
-    g.rb = __int_as_float(0x7F800000);
-  }
+  g.exact = g.s >= 0x1p-80f && g.s <= 0x1p+100f;
+  g.r = g.exact ? __frcp_rn(g.s) : 0.0f;
   return g;
 }
 
-// Codes of the pair (x0, x1) (x0 in the low byte) under multipliers ra2/rb2
-// (component k scales x_k).  ORs a nonzero value into `miss` when the two
-// brackets disagree, in which case the returned codes are not to be used.
-__device__ __forceinline__ uint32_t quant_pair_fast(float x0, float x1, float2 ra2, float2 rb2, uint32_t& miss) {
-  const float2 x = make_float2(x0, x1);
-  const float2 a = fmul2(x, ra2), b = fmul2(x, rb2);
-  const uint32_t ca = e4m3x2(a.x, a.y), cb = e4m3x2(b.x, b.y);
-  miss |= ca ^ cb;
-  return ca;
+// |v| with the sign of x.
+__device__ __forceinline__ float with_sign_of(float v, float x) {
+  return __uint_as_float((__float_as_uint(v) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// RN(x / s) for a pair, by the correction steps above (r2 = RN(1/s),
+// ns2 = -s, for each component).  The quotient has the sign of x (s > 0);
+// the sums of the correction steps would turn -0 (x = -0, or a quotient
+// that underflows) into +0, so the sign is taken from x.
+__device__ __forceinline__ float2 quotient_pair(float2 x, float2 r2, float2 ns2) {
+  float2 y = fmul2(x, r2);
+  y = ffma2(ffma2(y, ns2, x), r2, y);
+  const float2 q = ffma2(ffma2(y, ns2, x), r2, y);
+  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
+}
+
+// Codes of the pair (x0, x1) (x0 in the low byte), one group on the FMA path.
+__device__ __forceinline__ uint32_t quant_pair_exact(float x0, float x1, float2 r2, float2 ns2) {
+  const float2 q = quotient_pair(make_float2(x0, x1), r2, ns2);
+  return e4m3x2(q.x, q.y);
 }
 
 // Reference path: the IEEE quotient, then the cast.
@@ -234,19 +230,10 @@ __device__ __forceinline__ uint32_t quant_pair_div(float x0, float x1, float s0,
   return e4m3x2(__fdiv_rn(x0, s0), __fdiv_rn(x1, s1));
 }
 
-// The division paths are rare.  They live in separate, non-inlined
-// functions behind an unlikely branch, so that the compiler cannot turn
-// them into predicated code that every element would pay for.
-__device__ __noinline__ uint32_t quant_pair_div_call(float x0, float x1, float s) {
-  return quant_pair_div(x0, x1, s, s);
-}
-
 // Two codes (lo byte = a) of the values a, b under one group scale g.
 __device__ __forceinline__ uint32_t quant_pair(float a, float b, const GroupScale& g) {
-  uint32_t miss = 0;
-  const uint32_t c = quant_pair_fast(a, b, make_float2(g.ra, g.ra), make_float2(g.rb, g.rb), miss);
-  if (__builtin_expect(miss != 0u, 0)) return quant_pair_div_call(a, b, g.s);
-  return c;
+  if (g.exact) return quant_pair_exact(a, b, make_float2(g.r, g.r), make_float2(-g.s, -g.s));
+  return quant_pair_div(a, b, g.s, g.s);
 }
 
 __device__ __forceinline__ float warp_max(float v) {

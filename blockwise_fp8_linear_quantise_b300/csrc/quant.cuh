@@ -6,10 +6,9 @@
 // reduction dimension for activations and activation gradients, one per
 // 128x128 block for weights, each computed online from its own values.
 // Per group: amax = max|x| (NaN ignored); s = amax/448 in IEEE fp32 (1 when
-// amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  Codes come from the
-// bracketing products of GroupScale wherever those provably agree and from
-// the IEEE division otherwise, so codes and scales match a plain CPU
-// evaluation bit for bit.
+// amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  The quotient is formed
+// exactly by FMA correction steps (GroupScale), so codes and scales match a
+// plain CPU evaluation bit for bit.
 //
 // Work decomposition.  The input is cut into 128x128 bf16 tiles (32 KB),
 // walked in row-major order by a persistent grid (two CTAs per SM).  A CTA
@@ -23,14 +22,17 @@
 //     columns 16w+4(l%4)..+3 over rows 16(l/4)..16(l/4)+15.
 // It copies both slices into registers, releases the ring slot, reduces
 // amaxes with in-lane packed bf16 maxima and a few shuffles, turns each
-// amax into its scale once per warp instruction stream, and stores codes
+// amax into its scale and reciprocal once per warp instruction stream, forms
+// every code from the correctly rounded quotient (GroupScale), and stores codes
 // straight to global memory in 32-byte (rows) and 128-byte (columns)
 // segments.  The input is read from HBM once whichever outputs are requested.
 //
 // Shared-memory image of a tile: row r (256 bytes) starts at byte
-// 272 r + 16 ((r / 16) % 8).  The 16-byte stride padding and the per-block
-// offset make both register views conflict-free: 16 consecutive rows fall on
-// all eight 16-byte bank groups twice, and rows 16 apart on distinct ones.
+// 272 r + 32 ((r / 16) % 8).  The 16-byte stride padding and the per-block
+// offset make both register views conflict-free: in the row view 16
+// consecutive rows cover the eight 16-byte bank groups twice per half-warp;
+// in the column view rows 16 apart start 32 bytes (8 banks) apart, so eight
+// of them tile the 32 banks in two wavefronts, the minimum for 256 bytes.
 #pragma once
 
 #include "common.cuh"
@@ -51,13 +53,13 @@ constexpr int kQComputeWarps = 8;
 constexpr int kQuantThreads = 32 * kQComputeWarps;
 constexpr int kQStages = 3;
 constexpr int kQTileBytes = 128 * 256;                     // bf16 payload of a tile
-constexpr int kQBufBytes = 34944;                          // padded image, >= 272*127 + 16*7 + 256
+constexpr int kQBufBytes = 35072;                          // padded image, >= 272*127 + 32*7 + 256
 constexpr int kQBarOff = kQStages * kQBufBytes;            // full[3], empty[3], redbar[2]
 constexpr int kQRedOff = kQBarOff + (2 * kQStages + 2) * 8;  // float[2][8] (weight block amax)
 constexpr int kQuantSmemBytes = kQRedOff + 2 * kQComputeWarps * 4;
-static_assert(272 * 127 + 16 * 7 + 256 <= kQBufBytes, "tile image overflows its buffer");
+static_assert(272 * 127 + 32 * 7 + 256 <= kQBufBytes, "tile image overflows its buffer");
 
-__device__ __forceinline__ uint32_t qrow_off(int r) { return 272u * r + 16u * ((r >> 4) & 7); }
+__device__ __forceinline__ uint32_t qrow_off(int r) { return 272u * r + 32u * ((r >> 4) & 7); }
 
 __device__ __forceinline__ float bf16x2_absmax(uint32_t w) { return fmaxf(fabsf(bf16lo(w)), fabsf(bf16hi(w))); }
 
@@ -69,27 +71,26 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
   return d;
 }
 
-// 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i) by
-// the IEEE division: the rare path of quant16 / quant_col16 (not inlined,
-// so that its divisions are never predicated into the common path).
-__device__ __noinline__ uint4 quant16_div(uint4 a, uint4 b, float s) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i),
+// one group.  Groups with extreme scales (g.exact false) take the IEEE
+// division; the branch is uniform over the group.
+__device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
   uint32_t c[8];
+  if (g.exact) {
+    const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), s, s);
+    for (int i = 0; i < 8; ++i) c[i] = quant_pair_exact(bf16lo(w[i]), bf16hi(w[i]), r2, ns2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), g.s, g.s);
+  }
   return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
 // 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
 __device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
-  const float2 ra = make_float2(g.ra, g.ra), rb = make_float2(g.rb, g.rb);
-  uint32_t miss = 0;
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint32_t c[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = quant_pair_fast(bf16lo(w[i]), bf16hi(w[i]), ra, rb, miss);
-  if (__builtin_expect(miss != 0u, 0)) return quant16_div(a, b, g.s);
-  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+  return quant16w(w, g);
 }
 
 // Values k and k+1 of one column (element kHalf of word kWord of row slices
@@ -102,21 +103,11 @@ __device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
 
 // 16 codes of one column over 16 rows, one group.  Codes in row order.
 template <int kWord, int kHalf>
-__device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], float ra_, float rb_, float s) {
-  const float2 ra = make_float2(ra_, ra_), rb = make_float2(rb_, rb_);
-  uint32_t miss = 0, c[8];
+__device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupScale& g) {
+  uint32_t w[8];
 #pragma unroll
-  for (int k = 0; k < 16; k += 2) {
-    const uint32_t w0 = kWord ? v[k].y : v[k].x, w1 = kWord ? v[k + 1].y : v[k + 1].x;
-    c[k / 2] = quant_pair_fast(kHalf ? bf16hi(w0) : bf16lo(w0), kHalf ? bf16hi(w1) : bf16lo(w1), ra, rb, miss);
-  }
-  if (__builtin_expect(miss != 0u, 0)) {
-    uint32_t w[8];
-#pragma unroll
-    for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
-    return quant16_div(make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]), s);
-  }
-  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+  for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
+  return quant16w(w, g);
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
@@ -155,12 +146,14 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
     fence_mbar_init();
   }
   __syncthreads();
-  // prologue: the first kQStages tiles of this CTA
-  uint32_t issued = 0;  // tiles whose copies warp 0 has issued
+  // prologue: warp 0 issues the first kQStages tiles of this CTA, and later
+  // each tile j-1+kQStages at iteration j.
+  int64_t last_issued = -1;  // latest tile (local index) this warp issued after the prologue
+  uint32_t prologue = 0;     // tiles issued by the prologue (warp 0)
   if (warp == 0) {
     int64_t t = blockIdx.x;
-    for (int s = 0; s < kQStages && t < tiles; ++s, t += gridDim.x, ++issued)
-      quant_fill(p, t, ctiles, smem + s * kQBufBytes, &full[s], lane);
+    for (; prologue < kQStages && t < tiles; ++prologue, t += gridDim.x)
+      quant_fill(p, t, ctiles, smem + prologue * kQBufBytes, &full[prologue], lane);
   }
 
   const bool rows = p.q != nullptr, cols = p.qT != nullptr;
@@ -192,17 +185,17 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (warp == 0) {
-      // refill the slot of tile j-1 (every warp released it, usually long
-      // ago) with tile j-1+kQStages
+    if (warp == 0 && j >= 1) {
+      // Refill the slot of tile j-1 (every warp released it, usually long
+      // ago) with tile j-1+kQStages.
       const int64_t tn = t + (kQStages - 1) * static_cast<int64_t>(gridDim.x);
-      if (j >= 1 && tn < tiles) {
+      if (tn < tiles) {
         const uint32_t f = j - 1, sf = f % kQStages;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         quant_fill(p, tn, ctiles, smem + sf * kQBufBytes, &full[sf], lane);
-        ++issued;
+        last_issued = f + kQStages;
       }
     }
 
@@ -271,30 +264,33 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
     }
     if (cols) {
       // the scales of this lane's 4 columns live in lanes cq + 4k
-      float ra[4], rb[4], sc[4];
+      GroupScale gc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if constexpr (kWeight) {
-          ra[k] = gcol.ra;
-          rb[k] = gcol.rb;
-          sc[k] = gcol.s;
+          gc[k] = gcol;
         } else {
-          ra[k] = __shfl_sync(0xffffffffu, gcol.ra, cq + 4 * k);
-          rb[k] = __shfl_sync(0xffffffffu, gcol.rb, cq + 4 * k);
-          sc[k] = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
+          gc[k].s = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
+          gc[k].r = __shfl_sync(0xffffffffu, gcol.r, cq + 4 * k);
+          gc[k].exact = __shfl_sync(0xffffffffu, gcol.exact, cq + 4 * k);
         }
       }
       uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
-      *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0>(cv, ra[0], rb[0], sc[0]);
-      *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1>(cv, ra[1], rb[1], sc[1]);
-      *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0>(cv, ra[2], rb[2], sc[2]);
-      *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1>(cv, ra[3], rb[3], sc[3]);
+      *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0>(cv, gc[0]);
+      *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1>(cv, gc[1]);
+      *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0>(cv, gc[2]);
+      *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1>(cv, gc[3]);
     }
   }
   // Leave no copy in flight into this CTA's shared memory: after an early
-  // exit, wait (bounded) for the tiles issued but not consumed.
+  // exit at local tile j, warp 0 (which issues every copy) waits (bounded)
+  // for the tiles >= j it issued, at most kQStages of them.  No later fill
+  // of those slots can have been issued (that needs every warp to release
+  // the tile), so the waited phase is the one of that tile.  After a normal
+  // exit j counts all tiles of the CTA and nothing is waited for.
   if (warp == 0 && lane == 0) {
-    for (uint32_t k = j; k < issued; ++k)
+    const int64_t last = last_issued > static_cast<int64_t>(prologue) - 1 ? last_issued : static_cast<int64_t>(prologue) - 1;
+    for (int64_t k = j; k <= last; ++k)
       mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, p.wait_ns, kWeight ? 0x212u : 0x112u);
   }
 }
