@@ -128,6 +128,19 @@ bfp8_status make_kmajor_tmap(CUtensorMap* map, const void* base, int64_t rows, i
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
 }
 
+// bf16 [rows, cols] output, box 64 columns x 32 rows, 128-byte swizzle (the
+// GEMM epilogue's staging layout).
+bfp8_status make_bf16_store_tmap(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
+}
+
 struct GemmPlan {
   int bn;
   int m_tiles, n_tiles, tiles;
@@ -169,18 +182,18 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms) {
 }
 
 template <int BN>
-bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
-                           cudaStream_t st) {
+bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                           const GemmParams& p, int grid, cudaStream_t st) {
   const int smem = GemmSmem<BN>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_kernel<BN, kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      block_gemm_kernel<BN, kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_kernel<BN, kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      block_gemm_kernel<BN, kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+      block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -221,9 +234,10 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
     if (ws == nullptr || ws_bytes < g.ws_bytes) return BFP8_EWORKSPACE;
     if (!aligned16(ws)) return BFP8_EALIGN;
   }
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
   if ((s = make_kmajor_tmap(&tb, B, N, K, g.bn)) != BFP8_OK) return s;
+  if ((s = make_bf16_store_tmap(&tc, C, M, N)) != BFP8_OK) return s;
 
   GemmParams p;
   p.M = static_cast<int>(M);
@@ -249,8 +263,8 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   p.wait_ns = dev->wait_ns;
   const int mode = layout == BFP8_FPROP ? kSbBlock : (layout == BFP8_DGRAD ? kSbBlockT : kSbCol);
   const int grid = std::min(p.units, dev->sms);
-  s = g.bn == 256 ? launch_gemm_bn<256>(mode, ta, tb, p, grid, stream)
-                  : launch_gemm_bn<128>(mode, ta, tb, p, grid, stream);
+  s = g.bn == 256 ? launch_gemm_bn<256>(mode, ta, tb, tc, p, grid, stream)
+                  : launch_gemm_bn<128>(mode, ta, tb, tc, p, grid, stream);
   if (s != BFP8_OK) return s;
   if (g.splits == 1) {
     if (Cq == nullptr || fused_here) return BFP8_OK;

@@ -21,8 +21,9 @@
 //               slice's scale product and adds into 128 fp32 accumulators
 //               per thread held in registers, then frees the buffer.  While
 //               they promote slice kb the tensor core already computes kb+1.
-//               At the end of a tile they convert to bf16 (optionally also
-//               E4M3 codes of the bf16 output) and store.
+//               At the end of a tile they convert to bf16 and hand the
+//               tile to TMA stores through shared memory (or, with the
+//               fused E4M3 epilogue or split-K, store directly).
 //
 // The kernel is persistent: one CTA per SM walks work units (tile, split)
 // in a grouped order that keeps a band of A rows and B rows hot in L2.
@@ -69,15 +70,20 @@ constexpr int kLaunchRegs = 168;
 constexpr int kSmallRegs = 56;
 constexpr int kBigRegs = 224;
 static_assert(128 * kSmallRegs + 256 * kBigRegs <= kGemmThreads * kLaunchRegs, "register split exceeds the launch");
-constexpr int kStages = 4;
-
+// Shared memory of the GEMM: a ring of A (128x128) and B (BNx128) E4M3
+// tiles, the bf16 output staging for the TMA-store epilogue (each promotion
+// warp owns 32 rows x BN/2 columns, in boxes of 64 columns, 128-byte
+// swizzled), the per-column scale ring (WGRAD) and the barriers.
 template <int BN>
 struct GemmSmem {
+  static constexpr int kStages = BN == 256 ? 3 : 4;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kAOff = 0;
   static constexpr int kBOff = kStages * kABytes;
-  static constexpr int kRingOff = kBOff + kStages * kBBytes;  // float[2][BN] per-column scales
+  static constexpr int kCWarpBytes = 32 * (BN / 2) * 2;              // one promotion warp's staging
+  static constexpr int kCOff = kBOff + kStages * kBBytes;            // 1024-aligned
+  static constexpr int kRingOff = kCOff + 8 * kCWarpBytes;           // float[2][BN] per-column scales
   static constexpr int kBarOff = kRingOff + 2 * BN * 4;
   // barriers: full[S], empty[S], tfull[2], tempty[2], done, ring[2]
   static constexpr int kNumBars = 2 * kStages + 7;
@@ -85,6 +91,7 @@ struct GemmSmem {
   static constexpr int kBytes = kTmemSlotOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
   static constexpr uint32_t kTmemCols = 2 * BN;
+  static_assert(kAlloc <= 232448, "GEMM shared memory exceeds the per-CTA limit");
 };
 
 struct UnitCoords {
@@ -145,8 +152,9 @@ __device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], f
 template <int BN, int SBMODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using L = GemmSmem<BN>;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -182,6 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
   }
   tc_fence_before();
   __syncthreads();
@@ -361,7 +370,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if (p.splits == 1) {
+      if (p.splits == 1 && p.Cq == nullptr) {
+        // bf16 output through shared memory and TMA stores: this warp's 32
+        // rows x kCols columns go to its staging boxes (64 columns, 128-byte
+        // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), then lane
+        // 0 issues the stores and the warp moves on to the next tile.
+        uint8_t* stg = smem + L::kCOff + warp * L::kCWarpBytes;
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kCols / 8; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(stg + (i / 8) * 4096 + lane * 128 + (((i % 8) ^ (lane & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int bx = 0; bx < kCols / 64; ++bx) tma_store_2d(&tmC, stg + bx * 4096, col0 + 64 * bx, c.m0 + quad * 32);
+          bulk_commit_group();
+        }
+      } else if (p.splits == 1) {
         // bf16 output, 8 columns (16 bytes) per store.
         uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.N + col0;
         float m = 0.0f;
@@ -407,6 +442,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
 
+  // the staged output must have been read (and written) before the CTA ends
+  if (warp < kProducerWarp && lane == 0) bulk_wait_group<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
