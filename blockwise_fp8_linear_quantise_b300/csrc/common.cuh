@@ -209,20 +209,42 @@ __device__ __forceinline__ float with_sign_of(float v, float x) {
 }
 
 // RN(x / s) for a pair, by the correction steps above (r2 = RN(1/s),
-// ns2 = -s, for each component).  The quotient has the sign of x (s > 0);
-// the sums of the correction steps would turn -0 (x = -0, or a quotient
-// that underflows) into +0, so the sign is taken from x.
-__device__ __forceinline__ float2 quotient_pair(float2 x, float2 r2, float2 ns2) {
+// ns2 = -s, for each component), except that the sign of a zero result may
+// be lost (the sums of the correction steps turn -0 into +0).
+__device__ __forceinline__ float2 quotient_pair_unsigned_zero(float2 x, float2 r2, float2 ns2) {
   float2 y = fmul2(x, r2);
   y = ffma2(ffma2(y, ns2, x), r2, y);
-  const float2 q = ffma2(ffma2(y, ns2, x), r2, y);
-  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
+  return ffma2(ffma2(y, ns2, x), r2, y);
+}
+
+// Four E4M3 codes (byte i from q_i) in one register: two paired casts and
+// one pack.
+__device__ __forceinline__ uint32_t e4m3x4(float q0, float q1, float q2, float q3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(q0), "f"(q1), "f"(q2), "f"(q3));
+  return r;
+}
+
+// Codes of the four bf16 values of words w0, w1 (value 2i in the low half of
+// word i) in one group on the FMA path, byte k = value k.  The quotient has
+// the sign of x (s > 0), so the sign bits of the four inputs are ORed into
+// the codes: that restores -0 and changes nothing else.
+__device__ __forceinline__ uint32_t quant4_exact(uint32_t w0, uint32_t w1, float2 r2, float2 ns2) {
+  const float2 q0 = quotient_pair_unsigned_zero(make_float2(bf16lo(w0), bf16hi(w0)), r2, ns2);
+  const float2 q1 = quotient_pair_unsigned_zero(make_float2(bf16lo(w1), bf16hi(w1)), r2, ns2);
+  const uint32_t signs = __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+  return e4m3x4(q0.x, q0.y, q1.x, q1.y) | signs;
 }
 
 // Codes of the pair (x0, x1) (x0 in the low byte), one group on the FMA path.
 __device__ __forceinline__ uint32_t quant_pair_exact(float x0, float x1, float2 r2, float2 ns2) {
-  const float2 q = quotient_pair(make_float2(x0, x1), r2, ns2);
-  return e4m3x2(q.x, q.y);
+  const float2 q = quotient_pair_unsigned_zero(make_float2(x0, x1), r2, ns2);
+  return e4m3x2(with_sign_of(q.x, x0), with_sign_of(q.y, x1));
 }
 
 // Reference path: the IEEE quotient, then the cast.

@@ -75,15 +75,14 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
 // one group.  Groups with extreme scales (g.exact false) take the IEEE
 // division; the branch is uniform over the group.
 __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
-  uint32_t c[8];
   if (g.exact) {
     const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = quant_pair_exact(bf16lo(w[i]), bf16hi(w[i]), r2, ns2);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), g.s, g.s);
+    return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
+                      quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
   }
+  uint32_t c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), g.s, g.s);
   return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
