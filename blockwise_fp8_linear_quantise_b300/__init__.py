@@ -20,7 +20,7 @@ __all__ = ["ops", "workloads", "build"]
 
 _OPS = ("quantize_act_1x128", "quantize_w_128x128", "fp8_block_gemm", "linear_fwd", "linear_bwd",
         "gemm_workspace_bytes", "linear_fwd_workspace_bytes", "linear_bwd_workspace_bytes",
-        "sync_status", "set_wait_limit_ns", "set_gemm_splits", "launch_count", "FPROP", "DGRAD", "WGRAD")
+        "sync_status", "set_wait_limit_ns", "set_gemm_splits", "set_gemm_kernel", "launch_count", "FPROP", "DGRAD", "WGRAD")
 
 
 def __getattr__(name):

@@ -24,6 +24,7 @@ SIGNATURES = {
     "bfp8_linear_bwd_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "bfp8_sync_status": (c_int, [c_p]),
     "bfp8_set_wait_limit_ns": (c_int, [ctypes.c_uint64]),
+    "bfp8_set_gemm_kernel": (c_int, [c_int]),
     "bfp8_set_gemm_splits": (c_int, [c_int]),
     "bfp8_launch_count": (ctypes.c_uint64, []),
     "bfp8_status_string": (ctypes.c_char_p, [c_int]),

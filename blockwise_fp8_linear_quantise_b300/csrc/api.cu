@@ -28,12 +28,14 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   int sms = 0;
+  int pair_clusters = 0;  // co-resident clusters of the CTA-pair GEMM (0: not usable)
   uint64_t wait_ns = kDefaultWaitNs;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_forced_splits = 0;  // 0 = automatic
+int g_gemm_kind = 0;       // 0 = CTA pairs where the shape allows, 1 = single-CTA tiles only
 std::atomic<uint64_t> g_launches{0};  // kernels launched by this library
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -84,6 +86,14 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_SET_GEMM_SMEM(128, kSbBlockT)
     BFP8_SET_GEMM_SMEM(128, kSbCol)
 #undef BFP8_SET_GEMM_SMEM
+#define BFP8_SET_PAIR_SMEM(MODE)                                                                        \
+  if (e == cudaSuccess)                                                                                  \
+    e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             GemmSmem<256, true>::kAlloc);
+    BFP8_SET_PAIR_SMEM(kSbBlock)
+    BFP8_SET_PAIR_SMEM(kSbBlockT)
+    BFP8_SET_PAIR_SMEM(kSbCol)
+#undef BFP8_SET_PAIR_SMEM
     if (e != cudaSuccess) return BFP8_ECUDA;
     // The GEMM moves registers between warpgroups with setmaxnreg; that is
     // only safe if each thread really starts with kLaunchRegs registers.
@@ -102,6 +112,37 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_CHECK_REGS(128, kSbBlockT)
     BFP8_CHECK_REGS(128, kSbCol)
 #undef BFP8_CHECK_REGS
+#define BFP8_CHECK_PAIR_REGS(MODE)                                                   \
+  {                                                                                   \
+    cudaFuncAttributes fa;                                                            \
+    if (cudaFuncGetAttributes(&fa, block_gemm_pair_kernel<MODE>) != cudaSuccess) \
+      return BFP8_ECUDA;                                                              \
+    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                          \
+  }
+    BFP8_CHECK_PAIR_REGS(kSbBlock)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT)
+    BFP8_CHECK_PAIR_REGS(kSbCol)
+#undef BFP8_CHECK_PAIR_REGS
+    // How many CTA pairs can be resident at once (the persistent pair grid).
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(sms - (sms & 1)), 1, 1);
+      cfg.blockDim = dim3(kGemmThreads, 1, 1);
+      cfg.dynamicSmemBytes = GemmSmem<256, true>::kAlloc;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, block_gemm_pair_kernel<kSbBlock>, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // clear; the pair GEMM is then not used
+        clusters = 0;
+      }
+      st.pair_clusters = clusters;
+    }
     st.sms = sms;
     st.ready = true;
   }
@@ -142,32 +183,39 @@ bfp8_status make_bf16_store_tmap(CUtensorMap* map, void* base, int64_t rows, int
 }
 
 struct GemmPlan {
+  bool pair;                 // 256 x 256 tiles on CTA pairs
   int bn;
   int m_tiles, n_tiles, tiles;
   int splits, kps;
+  int slots;                 // work units that run at once
   size_t ws_bytes;
 };
 
-// Picks the column tile and the split-K factor.  Split-K only pays when the
-// tile count leaves SMs idle and the extra fp32 partial traffic is small next
-// to the GEMM time; estimate both with nominal B300 rates.
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sms) {
+// Picks the tile kind and the split-K factor.  CTA pairs (256 x 256 tiles)
+// are used for FPROP and DGRAD when both output dimensions allow them; WGRAD,
+// whose per-column scales double the promotion work, runs faster on
+// single-CTA 128 x BN tiles, as does any other shape.  Split-K only pays when the tile count leaves SMs idle and
+// the extra fp32 partial traffic is small next to the GEMM time; estimate both
+// with nominal B300 rates.
+GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const DeviceState& d) {
   GemmPlan g;
+  g.pair = g_gemm_kind == 0 && layout != BFP8_WGRAD && d.pair_clusters > 0 && M % 256 == 0 && N % 256 == 0;
   g.bn = (N % 256 == 0) ? 256 : 128;
-  g.m_tiles = static_cast<int>(M / 128);
+  g.m_tiles = static_cast<int>(M / (g.pair ? 256 : 128));
   g.n_tiles = static_cast<int>(N / g.bn);
   g.tiles = g.m_tiles * g.n_tiles;
+  g.slots = g.pair ? d.pair_clusters : d.sms;
   const int nk = static_cast<int>(K / 128);
   int best = 1;
   if (g_forced_splits > 0) {
     best = std::min(g_forced_splits, nk);
-  } else if (sms > 0) {
+  } else if (g.slots > 0) {
     const double t_gemm = 2.0 * M * N * K / 4.0e15;
     double best_t = 1e30;
     for (int s = 1; s <= std::min(nk, 16); ++s) {
       const int units = g.tiles * s;
-      const double waves = std::ceil(static_cast<double>(units) / sms);
-      const double eff = units / (waves * sms);
+      const double waves = std::ceil(static_cast<double>(units) / g.slots);
+      const double eff = units / (waves * g.slots);
       const double t = t_gemm / eff + (s > 1 ? (static_cast<double>(s) * M * N * 4 * 2 + M * N * 2) / 6.0e12 : 0.0);
       if (t < best_t * 0.97) {
         best_t = t;
@@ -194,6 +242,24 @@ bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& t
       break;
     default:
       block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      break;
+  }
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cuda_status(cudaGetLastError());
+}
+
+bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                             const GemmParams& p, int grid, cudaStream_t st) {
+  const int smem = GemmSmem<256, true>::kAlloc;
+  switch (mode) {
+    case kSbBlock:
+      block_gemm_pair_kernel<kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      break;
+    case kSbBlockT:
+      block_gemm_pair_kernel<kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      break;
+    default:
+      block_gemm_pair_kernel<kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -229,14 +295,14 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
-  const GemmPlan g = plan_gemm(M, N, K, dev->sms);
+  const GemmPlan g = plan_gemm(layout, M, N, K, *dev);
   if (g.ws_bytes > 0) {
     if (ws == nullptr || ws_bytes < g.ws_bytes) return BFP8_EWORKSPACE;
     if (!aligned16(ws)) return BFP8_EALIGN;
   }
   CUtensorMap ta, tb, tc;
   if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
-  if ((s = make_kmajor_tmap(&tb, B, N, K, g.bn)) != BFP8_OK) return s;
+  if ((s = make_kmajor_tmap(&tb, B, N, K, g.pair ? g.bn / 2 : g.bn)) != BFP8_OK) return s;
   if ((s = make_bf16_store_tmap(&tc, C, M, N)) != BFP8_OK) return s;
 
   GemmParams p;
@@ -249,7 +315,8 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   p.splits = g.splits;
   p.kps = g.kps;
   p.units = g.tiles * g.splits;
-  p.group_m = 16;
+  p.group_m = g.pair ? 8 : 16;
+  p.m_tile_rows = g.pair ? 256 : 128;
   p.sa = sa;
   p.sb = sb;
   p.C = static_cast<uint16_t*>(C);
@@ -262,9 +329,13 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   p.sCq = fused_here ? sCq : nullptr;
   p.wait_ns = dev->wait_ns;
   const int mode = layout == BFP8_FPROP ? kSbBlock : (layout == BFP8_DGRAD ? kSbBlockT : kSbCol);
-  const int grid = std::min(p.units, dev->sms);
-  s = g.bn == 256 ? launch_gemm_bn<256>(mode, ta, tb, tc, p, grid, stream)
-                  : launch_gemm_bn<128>(mode, ta, tb, tc, p, grid, stream);
+  if (g.pair) {
+    s = launch_gemm_pair(mode, ta, tb, tc, p, 2 * std::min(p.units, g.slots), stream);
+  } else {
+    const int grid = std::min(p.units, dev->sms);
+    s = g.bn == 256 ? launch_gemm_bn<256>(mode, ta, tb, tc, p, grid, stream)
+                    : launch_gemm_bn<128>(mode, ta, tb, tc, p, grid, stream);
+  }
   if (s != BFP8_OK) return s;
   if (g.splits == 1) {
     if (Cq == nullptr || fused_here) return BFP8_OK;
@@ -318,14 +389,14 @@ struct Carver {
   }
 };
 
-size_t fwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** Wq, uint8_t** Xq, float** sX,
+size_t fwd_ws(int64_t M, int64_t N, int64_t K, const DeviceState& sms, Carver* c, uint8_t** Wq, uint8_t** Xq, float** sX,
               void** gws) {
   Carver local(nullptr);
   Carver& cv = c ? *c : local;
   uint8_t* wq = cv.take<uint8_t>(static_cast<size_t>(N) * K);
   uint8_t* xq = cv.take<uint8_t>(static_cast<size_t>(M) * K);
   float* sx = cv.take<float>(static_cast<size_t>(K / 128) * M * sizeof(float));
-  const GemmPlan g = plan_gemm(M, N, K, sms);
+  const GemmPlan g = plan_gemm(BFP8_FPROP, M, N, K, sms);
   void* gw = cv.take<uint8_t>(g.ws_bytes);
   if (Wq) *Wq = wq;
   if (Xq) *Xq = xq;
@@ -334,7 +405,7 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** Wq,
   return cv.off;
 }
 
-size_t bwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** dYq, float** sdY, uint8_t** dYqT,
+size_t bwd_ws(int64_t M, int64_t N, int64_t K, const DeviceState& sms, Carver* c, uint8_t** dYq, float** sdY, uint8_t** dYqT,
               float** sdYT, void** gws) {
   Carver local(nullptr);
   Carver& cv = c ? *c : local;
@@ -342,8 +413,8 @@ size_t bwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** dYq
   float* b = cv.take<float>(static_cast<size_t>(N / 128) * M * sizeof(float));
   uint8_t* cT = cv.take<uint8_t>(static_cast<size_t>(N) * M);
   float* d = cv.take<float>(static_cast<size_t>(M / 128) * N * sizeof(float));
-  const GemmPlan gd = plan_gemm(M, K, N, sms);   // dgrad: [M, K], reduction N
-  const GemmPlan gw = plan_gemm(N, K, M, sms);   // wgrad: [N, K], reduction M
+  const GemmPlan gd = plan_gemm(BFP8_DGRAD, M, K, N, sms);  // dgrad: [M, K], reduction N
+  const GemmPlan gw = plan_gemm(BFP8_WGRAD, N, K, M, sms);  // wgrad: [N, K], reduction M
   void* w = cv.take<uint8_t>(std::max(gd.ws_bytes, gw.ws_bytes));
   if (dYq) *dYq = a;
   if (sdY) *sdY = b;
@@ -353,9 +424,15 @@ size_t bwd_ws(int64_t M, int64_t N, int64_t K, int sms, Carver* c, uint8_t** dYq
   return cv.off;
 }
 
-int current_sms() {
+// The current device's state, or a nominal B300 when it cannot be read (the
+// *_workspace_bytes() queries then still answer).
+DeviceState current_state() {
   DeviceState* dev = nullptr;
-  return device_state(&dev) == BFP8_OK ? dev->sms : 148;
+  if (device_state(&dev) == BFP8_OK) return *dev;
+  DeviceState d;
+  d.sms = 148;
+  d.pair_clusters = 74;
+  return d;
 }
 
 }  // namespace
@@ -405,7 +482,8 @@ bfp8_status bfp8_fp8_block_gemm_noalloc(bfp8_layout layout, const uint8_t* A, co
   void* scratch = nullptr;
   if ((s = noalloc_scratch(&scratch)) != BFP8_OK) return s;
   // The split-K partials of these sizes must fit in the static array.
-  if (plan_gemm(M, N, K, dev->sms).ws_bytes > static_cast<size_t>(BFP8_NOALLOC_SCRATCH_BYTES)) return BFP8_EWORKSPACE;
+  if (plan_gemm(layout, M, N, K, *dev).ws_bytes > static_cast<size_t>(BFP8_NOALLOC_SCRATCH_BYTES))
+    return BFP8_EWORKSPACE;
   return gemm_impl(layout, A, sa, B, sb, M, N, K, C, Cq, sCq, scratch, BFP8_NOALLOC_SCRATCH_BYTES,
                    reinterpret_cast<cudaStream_t>(stream));
 }
@@ -432,19 +510,18 @@ bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout, const uint8_t* A, const floa
 }
 
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K) {
-  (void)layout;
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
-  return plan_gemm(M, N, K, current_sms()).ws_bytes;
+  return plan_gemm(layout, M, N, K, current_state()).ws_bytes;
 }
 
 size_t bfp8_linear_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
-  return fwd_ws(M, N, K, current_sms(), nullptr, nullptr, nullptr, nullptr, nullptr);
+  return fwd_ws(M, N, K, current_state(), nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
-  return bwd_ws(M, N, K, current_sms(), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  return bwd_ws(M, N, K, current_state(), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
@@ -454,14 +531,14 @@ bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, 
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
-  const size_t need = fwd_ws(M, N, K, dev->sms, nullptr, nullptr, nullptr, nullptr, nullptr);
+  const size_t need = fwd_ws(M, N, K, *dev, nullptr, nullptr, nullptr, nullptr, nullptr);
   if (ws == nullptr || ws_bytes < need) return BFP8_EWORKSPACE;
   if (!aligned16(ws)) return BFP8_EALIGN;
   Carver cv(ws);
   uint8_t *Wq, *Xq;
   float* sX;
   void* gws;
-  fwd_ws(M, N, K, dev->sms, &cv, &Wq, &Xq, &sX, &gws);
+  fwd_ws(M, N, K, *dev, &cv, &Wq, &Xq, &sX, &gws);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = quant_w_impl(W, N, K, Wq, WqT, sW, st)) != BFP8_OK) return s;
   if ((s = quant_act_impl(X, M, K, Xq, sX, XqT, sXT, st)) != BFP8_OK) return s;
@@ -477,14 +554,14 @@ bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW,
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
-  const size_t need = bwd_ws(M, N, K, dev->sms, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  const size_t need = bwd_ws(M, N, K, *dev, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
   if (ws == nullptr || ws_bytes < need) return BFP8_EWORKSPACE;
   if (!aligned16(ws)) return BFP8_EALIGN;
   Carver cv(ws);
   uint8_t *dYq, *dYqT;
   float *sdY, *sdYT;
   void* gws;
-  bwd_ws(M, N, K, dev->sms, &cv, &dYq, &sdY, &dYqT, &sdYT, &gws);
+  bwd_ws(M, N, K, *dev, &cv, &dYq, &sdY, &dYqT, &sdYT, &gws);
   const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((s = quant_act_impl(dY, M, N, dYq, sdY, dYqT, sdYT, st)) != BFP8_OK) return s;
@@ -511,6 +588,13 @@ bfp8_status bfp8_set_wait_limit_ns(uint64_t ns) {
   if (s != BFP8_OK) return s;
   std::lock_guard<std::mutex> lk(g_mu);
   dev->wait_ns = ns == 0 ? kDefaultWaitNs : ns;
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_set_gemm_kernel(int kind) {
+  if (kind != 0 && kind != 1) return BFP8_EINVAL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_gemm_kind = kind;
   return BFP8_OK;
 }
 

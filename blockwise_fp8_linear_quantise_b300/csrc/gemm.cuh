@@ -48,6 +48,7 @@ struct GemmParams {
   int splits, kps;              // split-K count and slices per split
   int units;                    // tiles * splits
   int group_m;                  // tile rasterisation band height (in m tiles)
+  int m_tile_rows;              // rows per m tile: 128, or 256 for a CTA pair
   const float* sa;              // [K/128, M]
   const float* sb;              // see SbMode
   uint16_t* C;                  // bf16 [M, N] (splits == 1)
@@ -74,11 +75,13 @@ static_assert(128 * kSmallRegs + 256 * kBigRegs <= kGemmThreads * kLaunchRegs, "
 // tiles, the bf16 output staging for the TMA-store epilogue (each promotion
 // warp owns 32 rows x BN/2 columns, in boxes of 64 columns, 128-byte
 // swizzled), the per-column scale ring (WGRAD) and the barriers.
-template <int BN>
+// With kPair the CTA is one of a pair sharing a 256 x BN tile: it holds its
+// own 128 rows of A and half (BN/2 rows) of B per stage.
+template <int BN, bool kPair = false>
 struct GemmSmem {
-  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kStages = kPair ? 4 : (BN == 256 ? 3 : 4);
   static constexpr int kABytes = 128 * 128;
-  static constexpr int kBBytes = BN * 128;
+  static constexpr int kBBytes = (kPair ? BN / 2 : BN) * 128;
   static constexpr int kAOff = 0;
   static constexpr int kBOff = kStages * kABytes;
   static constexpr int kCWarpBytes = 32 * (BN / 2) * 2;              // one promotion warp's staging
@@ -110,7 +113,7 @@ __device__ __forceinline__ UnitCoords unit_coords(const GemmParams& p, int u) {
   const int first_m = g * p.group_m;
   const int gm = min(p.m_tiles - first_m, p.group_m);
   const int in_g = tile - g * per_group;
-  c.m0 = (first_m + in_g % gm) * 128;
+  c.m0 = (first_m + in_g % gm) * p.m_tile_rows;
   c.nt = in_g / gm;
   const int nk = p.K / 128;
   c.kb0 = c.split * p.kps;
@@ -149,11 +152,16 @@ __device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], f
   }
 }
 
-template <int BN, int SBMODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = GemmSmem<BN>;
+// The GEMM body.  kPair: this CTA and its cluster peer compute a 256 x BN
+// tile together with tcgen05 pair MMAs (cta_group::2): each loads its own
+// 128 rows of A and BN/2 rows of B (so each SM moves 32 KB per slice instead
+// of 48 KB), the first CTA of the pair issues the MMAs, whose results land in
+// both CTAs' tensor memory (each CTA its own 128 rows x BN columns), and each
+// CTA promotes and stores its own rows.
+template <int BN, int SBMODE, bool kPair>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                                          const GemmParams& p) {
+  using L = GemmSmem<BN, kPair>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -168,6 +176,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   float* ring = reinterpret_cast<float*>(smem + L::kRingOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: this CTA issues the MMAs
+  const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // one arrival per promotion warp
+      mbar_init(&tempty[b], kPair ? 16 : 8);  // one arrival per promotion warp (of both CTAs)
     }
     mbar_init(done, 1);
     mbar_init(&ringbar[0], 256);
@@ -184,8 +195,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, L::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, L::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, L::kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&tmA);
@@ -194,6 +210,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before either CTA signals them
+  if constexpr (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -204,33 +222,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const UnitCoords c = unit_coords(p, u);
+      for (int u = unit0; u < p.units && ok; u += unit_step) {
+        UnitCoords c = unit_coords(p, u);
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, 0x301u)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], L::kABytes + L::kBBytes);
-          tma_load_2d(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, c.m0, &full[s]);
-          tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128, c.nt * BN, &full[s]);
+          if constexpr (kPair) {
+            // both CTAs' copies are counted on the first CTA's full[s]
+            const uint32_t leader_full = mapa_shared(&full[s], 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (L::kABytes + L::kBBytes));
+            tma_load_2d_pair(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, c.m0 + 128 * static_cast<int>(rank),
+                             leader_full);
+            tma_load_2d_pair(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128,
+                             c.nt * BN + (BN / 2) * static_cast<int>(rank), leader_full);
+          } else {
+            mbar_arrive_expect_tx(&full[s], L::kABytes + L::kBBytes);
+            tma_load_2d(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, c.m0, &full[s]);
+            tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128, c.nt * BN, &full[s]);
+          }
         }
       }
       // Do not leave while copies into this CTA's shared memory are in flight:
-      // wait for the last fill of every stage to land.
-      for (uint32_t j = 0; j < kStages && j < it; ++j) {
-        const uint32_t f = it - 1 - j;
-        mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
+      // wait for the last fill of every stage to land (for a pair, the first
+      // CTA's full barriers count both CTAs' copies; the second CTA is held
+      // by the cluster barrier at the end until the first is done).
+      if (!kPair || rank == 0) {
+        for (uint32_t j = 0; j < kStages && j < it; ++j) {
+          const uint32_t f = it - 1 - j;
+          mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
+        }
       }
     }
     } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(128, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kPair ? 256 : 128, BN);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int u = unit0; u < p.units && ok; u += unit_step) {
         const UnitCoords c = unit_coords(p, u);
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -243,15 +275,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_addr = smem_u32(smem + L::kAOff + s * L::kABytes);
           const uint32_t b_addr = smem_u32(smem + L::kBOff + s * L::kBBytes);
           const uint32_t d = tmem_base + b * BN;
+          if constexpr (kPair) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_e4m3(d, sw128_kmajor_desc(a_addr + 32 * k), sw128_kmajor_desc(b_addr + 32 * k), idesc, k > 0);
-          mma_commit(&empty[s]);
-          mma_commit(&tfull[b]);
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3_pair(d, sw128_kmajor_desc(a_addr + 32 * k), sw128_kmajor_desc(b_addr + 32 * k), idesc, k > 0);
+            mma_commit_pair_mc(&empty[s], 0x3);
+            mma_commit_pair_mc(&tfull[b], 0x3);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_e4m3(d, sw128_kmajor_desc(a_addr + 32 * k), sw128_kmajor_desc(b_addr + 32 * k), idesc, k > 0);
+            mma_commit(&empty[s]);
+            mma_commit(&tfull[b]);
+          }
         }
       }
       // Every MMA this thread issued has completed once `done` fires.
-      mma_commit(done);
+      if constexpr (kPair) {
+        mma_commit_pair_mc(done, 0x1);
+      } else {
+        mma_commit(done);
+      }
       mbar_wait(done, 0, p.wait_ns, 0x313u);
     }
     }
@@ -266,8 +310,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     float acc[kCols];
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const UnitCoords c = unit_coords(p, u);
+    // where this warp reports a freed TMEM buffer: the first CTA's tempty
+    const uint32_t tempty_leader0 = kPair ? mapa_shared(&tempty[0], 0) : 0u;
+    const uint32_t tempty_leader1 = kPair ? mapa_shared(&tempty[1], 0) : 0u;
+    for (int u = unit0; u < p.units && ok; u += unit_step) {
+      UnitCoords c = unit_coords(p, u);
+      c.m0 += 128 * static_cast<int>(rank);  // this CTA's rows of a pair tile
       const int gm = c.m0 + row;
       const int col0 = c.nt * BN + half * kCols;  // first output column of this thread
 #pragma unroll
@@ -330,33 +378,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + b * BN + half * kCols;
-        // acc[j] += P[j] * scale(j) over this thread's kCols columns, read from
-        // TMEM in 32-column chunks: the load of chunk c+1 is in flight while
-        // chunk c is multiplied in.  The buffer is released as soon as its
-        // last chunk is in registers.
+        // acc[j] += P[j] * scale(j) over this thread's kCols columns, read
+        // from TMEM 64 columns at a time: each tcgen05.ld round trip is
+        // long next to the FMAs it feeds, and tcgen05.wait::ld drains every
+        // outstanding load, so fewer, wider loads shorten the chain.  The
+        // buffer is released as soon as its last chunk is in registers.
         const float s = sa_cur * sb_cur;
         const float2 s2 = make_float2(s, s);
         const float2 sa2 = make_float2(sa_cur, sa_cur);
         const float* sbc = ring + b * BN + half * kCols;
-        uint32_t va[32], vb[32];
-        tmem_ld32(taddr, va);
-        tmem_wait_ld32(va);
 #pragma unroll
-        for (int ch = 0; ch < kCols / 32; ch += 2) {
-          tmem_ld32(taddr + (ch + 1) * 32, vb);
-          promote32<SBMODE>(acc + ch * 32, va, s2, sa2, sbc + ch * 32);
-          reg_fence32(acc + ch * 32);
-          tmem_wait_ld32(vb);
-          if (ch + 2 < kCols / 32) {
-            tmem_ld32(taddr + (ch + 2) * 32, va);
-          } else {
+        for (int ch = 0; ch < kCols / 64; ++ch) {
+          uint32_t v[64];
+          tmem_ld64(taddr + ch * 64, v);
+          tmem_wait_ld64(v);
+          if (ch + 1 == kCols / 64) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (lane == 0) {
+              if (kPair && rank != 0)
+                mbar_arrive_cluster(b ? tempty_leader1 : tempty_leader0);
+              else
+                mbar_arrive(&tempty[b]);
+            }
           }
-          promote32<SBMODE>(acc + (ch + 1) * 32, vb, s2, sa2, sbc + (ch + 1) * 32);
-          reg_fence32(acc + (ch + 1) * 32);
-          if (ch + 2 < kCols / 32) tmem_wait_ld32(va);
+          promote32<SBMODE>(acc + ch * 64, *reinterpret_cast<const uint32_t(*)[32]>(v), s2, sa2, sbc + ch * 64);
+          promote32<SBMODE>(acc + ch * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32), s2, sa2,
+                            sbc + ch * 64 + 32);
+          reg_fence64(acc + ch * 64);
         }
         if constexpr (SBMODE == kSbCol) {
           // Everyone has passed this slice's ring wait, so every thread is
@@ -446,10 +495,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp < kProducerWarp && lane == 0) bulk_wait_group<0>();
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair may leave (or free tensor memory) while the other
+  // can still signal its barriers or read its shared memory
+  if constexpr (kPair) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, L::kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, L::kTmemCols);
   }
+}
+
+template <int BN, int SBMODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  gemm_body<BN, SBMODE, false>(tmA, tmB, tmC, p);
+}
+
+// 256 x 256 output tiles on CTA pairs (clusters of two).
+template <int SBMODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    block_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  gemm_body<256, SBMODE, true>(tmA, tmB, tmC, p);
 }
 
 // Adds the fp32 split-K partials in split order, rounds to bf16 and,

@@ -189,6 +189,11 @@ def set_wait_limit_ns(ns):
     _check(_lib.load().bfp8_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
 
 
+def set_gemm_kernel(kind):
+    """0: CTA-pair 256x256 tiles where the shape allows (default); 1: single-CTA tiles only."""
+    _check(_lib.load().bfp8_set_gemm_kernel(int(kind)), "set_gemm_kernel")
+
+
 def set_gemm_splits(splits):
     _check(_lib.load().bfp8_set_gemm_splits(int(splits)), "set_gemm_splits")
 

@@ -218,6 +218,17 @@ bfp8_status bfp8_sync_status(bfp8_stream_t stream);
 bfp8_status bfp8_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Selects the GEMM tiling for every later call in the process: 0 (default)
+ * uses 256 x 256 output tiles computed by pairs of CTAs (tensor-core pair
+ * MMAs) for FPROP and DGRAD whenever both output dimensions are multiples of
+ * 256, and 128 x 256 (or 128 x 128) single-CTA tiles otherwise (always for
+ * WGRAD); 1 always uses single-CTA tiles.
+ * Both give results within the same tolerance of the oracle.
+ * Errors: EINVAL for any other value.
+ */
+bfp8_status bfp8_set_gemm_kernel(int kind);
+
+/*
  * Overrides the split-K factor the GEMM picks (0 restores the automatic
  * choice, which splits the reduction only when that fills idle SMs at a
  * lower cost than the extra fp32 partial traffic).  Applies to every later

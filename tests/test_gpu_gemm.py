@@ -71,12 +71,37 @@ def rand_layer(M, N, K, seed):
     return np32(X), np32(W), np32(dY)
 
 
+@pytest.fixture(params=[0, 1], ids=["pair-tiles", "single-cta-tiles"])
+def gemm_kind(request):
+    """Run a test with the CTA-pair GEMM (where the shape allows) and with
+    single-CTA tiles only."""
+    ops.set_gemm_kernel(request.param)
+    yield request.param
+    ops.set_gemm_kernel(0)
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (384, 640, 512), (512, 768, 384), (1024, 1280, 1536),
-                                   (128, 128, 128), (2304, 512, 640)])
-def test_small_shapes_all_layouts(M, N, K):
+                                   (128, 128, 128), (2304, 512, 640), (768, 1024, 2048)])
+def test_small_shapes_all_layouts(M, N, K, gemm_kind):
     X, W, dY = rand_layer(M, N, K, M + N + K)
     o = quantised_layer(X, W, dY)
     run_layouts(o, ["fprop", "dgrad", "wgrad"])
+
+
+def test_pair_and_single_tiles_agree():
+    """Both tilings accumulate the same slices in the same order, so their
+    bf16 outputs agree to rounding of the tensor-core partial sums."""
+    X, W, dY = rand_layer(1024, 1536, 2048, 11)
+    o = quantised_layer(X, W, dY)
+    outs = []
+    for kind in (0, 1):
+        try:
+            ops.set_gemm_kernel(kind)
+            outs.append(np32(ops.fp8_block_gemm(ops.FPROP, gpu(o, "Xq"), gpu(o, "sX"), gpu(o, "Wq"), gpu(o, "sW"))))
+        finally:
+            ops.set_gemm_kernel(0)
+    assert ops.sync_status() == 0
+    assert rel_fro(outs[0], outs[1]) <= 1e-4
 
 
 def test_tiny_config():
@@ -91,7 +116,7 @@ def test_tiny_config():
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 5])
-def test_forced_split_k(splits):
+def test_forced_split_k(splits, gemm_kind):
     X, W, dY = rand_layer(640, 512, 768, 99)
     o = quantised_layer(X, W, dY)
     try:
@@ -102,7 +127,7 @@ def test_forced_split_k(splits):
 
 
 @pytest.mark.parametrize("splits", [1, 3])
-def test_fused_quantised_epilogue(splits):
+def test_fused_quantised_epilogue(splits, gemm_kind):
     X, W, dY = rand_layer(512, 768, 640, 5)
     o = quantised_layer(X, W, dY)
     try:
