@@ -86,6 +86,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--probe-fp8-peak", action="store_true",
+                    help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
     return ap.parse_args(argv)
 
 
@@ -648,8 +650,56 @@ def gpu_arm(args):
     return 0
 
 
+def fp8_peak_probe():
+    """Dense FP8 GEMM throughput of the vendor library on this GPU: 8192^3
+    E4M3 x E4M3 with per-tensor scales, bf16 out.  Best of 10 (burst) and a
+    4-second back-to-back loop (sustained), with the clocks seen meanwhile."""
+    import torch
+    n = 8192
+    dev = torch.device("cuda")
+    a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device=dev)
+    mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(3):
+        mm()
+    torch.cuda.synchronize()
+    best = 1e30
+    for _ in range(10):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    clocks = ClockSampler(gpu_uuid(dev))
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    reps = 0
+    e0.record()
+    while time.perf_counter() - t0 < 4.0:
+        for _ in range(20):
+            mm()
+        reps += 20
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    flop = 2.0 * n ** 3
+    line = {"probe": "fp8_dense_peak", "how": "torch._scaled_mm e4m3 8192^3 per-tensor scales, bf16 out",
+            "burst_tflops": flop / (best * 1e-3) / 1e12,
+            "sustained_tflops": flop * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.probe_fp8_peak:
+        return fp8_peak_probe()
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

@@ -67,61 +67,79 @@ bfp8_status device_state(DeviceState** out) {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     cudaError_t e = cudaSuccess;
-    e = cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes);
     // two quantiser CTAs per SM need the largest shared-memory carveout
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(quantize_tile_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(quantize_tile_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-#define BFP8_SET_GEMM_SMEM(BN, MODE)                                                                     \
-  if (e == cudaSuccess)                                                                                   \
-    e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define BFP8_SET_QUANT_SMEM(W, MODE)                                                                           \
+  if (e == cudaSuccess)                                                                                         \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+                             kQuantSmemBytes);                                                                  \
+  if (e == cudaSuccess)                                                                                         \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    BFP8_SET_QUANT_SMEM(false, kQRows)
+    BFP8_SET_QUANT_SMEM(false, kQCols)
+    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols)
+    BFP8_SET_QUANT_SMEM(true, kQRows)
+    BFP8_SET_QUANT_SMEM(true, kQCols)
+    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols)
+#undef BFP8_SET_QUANT_SMEM
+#define BFP8_SET_GEMM_SMEM(BN, MODE, FUSED)                                                                     \
+  if (e == cudaSuccess)                                                                                          \
+    e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              GemmSmem<BN>::kAlloc);
-    BFP8_SET_GEMM_SMEM(256, kSbBlock)
-    BFP8_SET_GEMM_SMEM(256, kSbBlockT)
-    BFP8_SET_GEMM_SMEM(256, kSbCol)
-    BFP8_SET_GEMM_SMEM(128, kSbBlock)
-    BFP8_SET_GEMM_SMEM(128, kSbBlockT)
-    BFP8_SET_GEMM_SMEM(128, kSbCol)
+    BFP8_SET_GEMM_SMEM(256, kSbBlock, false)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT, false)
+    BFP8_SET_GEMM_SMEM(256, kSbCol, false)
+    BFP8_SET_GEMM_SMEM(256, kSbBlock, true)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT, true)
+    BFP8_SET_GEMM_SMEM(256, kSbCol, true)
+    BFP8_SET_GEMM_SMEM(128, kSbBlock, false)
+    BFP8_SET_GEMM_SMEM(128, kSbBlockT, false)
+    BFP8_SET_GEMM_SMEM(128, kSbCol, false)
 #undef BFP8_SET_GEMM_SMEM
-#define BFP8_SET_PAIR_SMEM(MODE)                                                                        \
-  if (e == cudaSuccess)                                                                                  \
-    e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define BFP8_SET_PAIR_SMEM(MODE, FUSED)                                                                        \
+  if (e == cudaSuccess)                                                                                         \
+    e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              GemmSmem<256, true>::kAlloc);
-    BFP8_SET_PAIR_SMEM(kSbBlock)
-    BFP8_SET_PAIR_SMEM(kSbBlockT)
-    BFP8_SET_PAIR_SMEM(kSbCol)
+    BFP8_SET_PAIR_SMEM(kSbBlock, false)
+    BFP8_SET_PAIR_SMEM(kSbBlockT, false)
+    BFP8_SET_PAIR_SMEM(kSbCol, false)
+    BFP8_SET_PAIR_SMEM(kSbBlock, true)
+    BFP8_SET_PAIR_SMEM(kSbBlockT, true)
+    BFP8_SET_PAIR_SMEM(kSbCol, true)
 #undef BFP8_SET_PAIR_SMEM
     if (e != cudaSuccess) return BFP8_ECUDA;
     // The GEMM moves registers between warpgroups with setmaxnreg; that is
     // only safe if each thread really starts with kLaunchRegs registers.
     // Refuse to run a build where it does not (it would wait forever).
-#define BFP8_CHECK_REGS(BN, MODE)                                                  \
-  {                                                                                 \
-    cudaFuncAttributes fa;                                                          \
-    if (cudaFuncGetAttributes(&fa, block_gemm_kernel<BN, MODE>) != cudaSuccess) \
-      return BFP8_ECUDA;                                                            \
-    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                        \
+#define BFP8_CHECK_REGS(BN, MODE, FUSED)                                                  \
+  {                                                                                        \
+    cudaFuncAttributes fa;                                                                 \
+    if (cudaFuncGetAttributes(&fa, block_gemm_kernel<BN, MODE, FUSED>) != cudaSuccess) \
+      return BFP8_ECUDA;                                                                   \
+    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                               \
   }
-    BFP8_CHECK_REGS(256, kSbBlock)
-    BFP8_CHECK_REGS(256, kSbBlockT)
-    BFP8_CHECK_REGS(256, kSbCol)
-    BFP8_CHECK_REGS(128, kSbBlock)
-    BFP8_CHECK_REGS(128, kSbBlockT)
-    BFP8_CHECK_REGS(128, kSbCol)
+    BFP8_CHECK_REGS(256, kSbBlock, false)
+    BFP8_CHECK_REGS(256, kSbBlockT, false)
+    BFP8_CHECK_REGS(256, kSbCol, false)
+    BFP8_CHECK_REGS(256, kSbBlock, true)
+    BFP8_CHECK_REGS(256, kSbBlockT, true)
+    BFP8_CHECK_REGS(256, kSbCol, true)
+    BFP8_CHECK_REGS(128, kSbBlock, false)
+    BFP8_CHECK_REGS(128, kSbBlockT, false)
+    BFP8_CHECK_REGS(128, kSbCol, false)
 #undef BFP8_CHECK_REGS
-#define BFP8_CHECK_PAIR_REGS(MODE)                                                   \
-  {                                                                                   \
-    cudaFuncAttributes fa;                                                            \
-    if (cudaFuncGetAttributes(&fa, block_gemm_pair_kernel<MODE>) != cudaSuccess) \
-      return BFP8_ECUDA;                                                              \
-    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                          \
+#define BFP8_CHECK_PAIR_REGS(MODE, FUSED)                                                   \
+  {                                                                                          \
+    cudaFuncAttributes fa;                                                                   \
+    if (cudaFuncGetAttributes(&fa, block_gemm_pair_kernel<MODE, FUSED>) != cudaSuccess) \
+      return BFP8_ECUDA;                                                                     \
+    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                                 \
   }
-    BFP8_CHECK_PAIR_REGS(kSbBlock)
-    BFP8_CHECK_PAIR_REGS(kSbBlockT)
-    BFP8_CHECK_PAIR_REGS(kSbCol)
+    BFP8_CHECK_PAIR_REGS(kSbBlock, false)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT, false)
+    BFP8_CHECK_PAIR_REGS(kSbCol, false)
+    BFP8_CHECK_PAIR_REGS(kSbBlock, true)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT, true)
+    BFP8_CHECK_PAIR_REGS(kSbCol, true)
 #undef BFP8_CHECK_PAIR_REGS
     // How many CTA pairs can be resident at once (the persistent pair grid).
     {
@@ -164,6 +182,20 @@ bfp8_status make_kmajor_tmap(CUtensorMap* map, const void* base, int64_t rows, i
   cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
+}
+
+// The quantisers' input x [R, C] bf16 seen as the 2-D tensor [R/16, 16 C]
+// (row y = input rows 16y..16y+15 side by side), box 64 elements x 8 rows,
+// 128-byte swizzle: one box brings 64 columns of 8 input rows 16 apart.
+bfp8_status make_quant_tmap(CUtensorMap* map, const void* x, int64_t R, int64_t C) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(16 * C), static_cast<cuuint64_t>(R / 16)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(32 * C)};
+  cuuint32_t box[2] = {64, 8};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
@@ -229,55 +261,96 @@ GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const De
   return g;
 }
 
-template <int BN>
-bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                           const GemmParams& p, int grid, cudaStream_t st) {
+template <int BN, bool kFused>
+void launch_gemm_bn_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                         const GemmParams& p, int grid, cudaStream_t st) {
   const int smem = GemmSmem<BN>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_kernel<BN, kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlock, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_kernel<BN, kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlockT, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_kernel<BN, kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbCol, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
+  }
+}
+
+// p.Cq set (one split, BN = 256 only) selects the instance with the fused
+// E4M3 epilogue.
+template <int BN>
+bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                           const GemmParams& p, int grid, cudaStream_t st) {
+  if constexpr (BN == 256) {
+    if (p.Cq != nullptr)
+      launch_gemm_bn_mode<BN, true>(mode, ta, tb, tc, p, grid, st);
+    else
+      launch_gemm_bn_mode<BN, false>(mode, ta, tb, tc, p, grid, st);
+  } else {
+    if (p.Cq != nullptr) return BFP8_EINVAL;
+    launch_gemm_bn_mode<BN, false>(mode, ta, tb, tc, p, grid, st);
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
-bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                             const GemmParams& p, int grid, cudaStream_t st) {
+template <bool kFused>
+void launch_gemm_pair_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                           const GemmParams& p, int grid, cudaStream_t st) {
   const int smem = GemmSmem<256, true>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_pair_kernel<kSbBlock><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlock, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_pair_kernel<kSbBlockT><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlockT, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_pair_kernel<kSbCol><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbCol, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
   }
+}
+
+bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                             const GemmParams& p, int grid, cudaStream_t st) {
+  if (p.Cq != nullptr)
+    launch_gemm_pair_mode<true>(mode, ta, tb, tc, p, grid, st);
+  else
+    launch_gemm_pair_mode<false>(mode, ta, tb, tc, p, grid, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
 // Persistent quantiser grid: two CTAs per SM (each streams its tiles
-// through a 3-deep shared-memory ring).
-bfp8_status launch_quant(const QuantParams& p, bool weight, cudaStream_t st) {
+// through a 3-deep shared-memory ring).  The tile walk and the TMA
+// coordinates are 32-bit: C up to 2^27 and fewer than 2^31 tiles.
+template <bool kWeight>
+bfp8_status launch_quant_mode(const CUtensorMap& tm, const QuantParams& p, unsigned grid, cudaStream_t st) {
+  const int mode = (p.q ? kQRows : 0) | (p.qT ? kQCols : 0);
+  if (mode == kQRows)
+    quantize_tile_kernel<kWeight, kQRows><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+  else if (mode == kQCols)
+    quantize_tile_kernel<kWeight, kQCols><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+  else
+    quantize_tile_kernel<kWeight, kQRows | kQCols><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+  return BFP8_OK;
+}
+
+bfp8_status launch_quant(QuantParams p, bool weight, cudaStream_t st) {
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
+  if (p.q == nullptr && p.qT == nullptr) return BFP8_EINVAL;
   const int64_t tiles = (p.R / 128) * (p.C / 128);
+  if (p.C > (int64_t(1) << 27) || tiles >= (int64_t(1) << 31)) return BFP8_EINVAL;
+  p.ctiles = static_cast<uint32_t>(p.C / 128);
+  p.tiles = static_cast<uint32_t>(tiles);
+  CUtensorMap tm;
+  if ((s = make_quant_tmap(&tm, p.x, p.R, p.C)) != BFP8_OK) return s;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
-  if (weight)
-    quantize_tile_kernel<true><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
-  else
-    quantize_tile_kernel<false><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(p);
+  s = weight ? launch_quant_mode<true>(tm, p, grid, st) : launch_quant_mode<false>(tm, p, grid, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -339,7 +412,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   if (s != BFP8_OK) return s;
   if (g.splits == 1) {
     if (Cq == nullptr || fused_here) return BFP8_OK;
-    QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns};
+    QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns, 0u, 0u};
     return launch_quant(qp, false, stream);
   }
   const int64_t groups = M * (N / 128);
@@ -360,7 +433,7 @@ bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, floa
   DeviceState* dev = nullptr;
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
-  QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns};
+  QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns, 0u, 0u};
   return launch_quant(p, false, stream);
 }
 
@@ -371,7 +444,7 @@ bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_
   DeviceState* dev = nullptr;
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
-  QuantParams p{static_cast<const uint16_t*>(w), N, K, q, s, qT, nullptr, dev->wait_ns};
+  QuantParams p{static_cast<const uint16_t*>(w), N, K, q, s, qT, nullptr, dev->wait_ns, 0u, 0u};
   return launch_quant(p, true, stream);
 }
 

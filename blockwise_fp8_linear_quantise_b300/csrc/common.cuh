@@ -127,6 +127,22 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ------------------------------------------------ non-bulk async copies
+// cp.async of 16 (or 4) bytes global -> shared; both addresses aligned to
+// the size.  Completion is reported to an mbarrier by cp_async_arrive.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued so far has landed
+// (.noinc: the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Makes generic-proxy writes to shared memory visible to the async proxy
 // (needed before a TMA store reads what threads wrote).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -74,7 +74,9 @@ static_assert(128 * kSmallRegs + 256 * kBigRegs <= kGemmThreads * kLaunchRegs, "
 // Shared memory of the GEMM: a ring of A (128x128) and B (BNx128) E4M3
 // tiles, the bf16 output staging for the TMA-store epilogue (each promotion
 // warp owns 32 rows x BN/2 columns, in boxes of 64 columns, 128-byte
-// swizzled), the per-column scale ring (WGRAD) and the barriers.
+// swizzled), the scale ring and the barriers.  Scale slot i holds the scales
+// of one slice: sa of this CTA's 128 rows, then sb (the slice's block
+// scalars of the tile's column blocks, or its BN per-column scales).
 // With kPair the CTA is one of a pair sharing a 256 x BN tile: it holds its
 // own 128 rows of A and half (BN/2 rows) of B per stage.
 template <int BN, bool kPair = false>
@@ -86,10 +88,12 @@ struct GemmSmem {
   static constexpr int kBOff = kStages * kABytes;
   static constexpr int kCWarpBytes = 32 * (BN / 2) * 2;              // one promotion warp's staging
   static constexpr int kCOff = kBOff + kStages * kBBytes;            // 1024-aligned
-  static constexpr int kRingOff = kCOff + 8 * kCWarpBytes;           // float[2][BN] per-column scales
-  static constexpr int kBarOff = kRingOff + 2 * BN * 4;
-  // barriers: full[S], empty[S], tfull[2], tempty[2], done, ring[2]
-  static constexpr int kNumBars = 2 * kStages + 7;
+  static constexpr int kScaleSlots = 8;                              // > kStages + 2: never the limit
+  static constexpr int kScaleSlotFloats = 128 + BN;
+  static constexpr int kScaleOff = kCOff + 8 * kCWarpBytes;
+  static constexpr int kBarOff = kScaleOff + kScaleSlots * kScaleSlotFloats * 4;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], done, sfull[8], sempty[8]
+  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kScaleSlots;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlotOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -158,7 +162,7 @@ __device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], f
 // of 48 KB), the first CTA of the pair issues the MMAs, whose results land in
 // both CTAs' tensor memory (each CTA its own 128 rows x BN columns), and each
 // CTA promotes and stores its own rows.
-template <int BN, int SBMODE, bool kPair>
+template <int BN, int SBMODE, bool kPair, bool kFused>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                           const GemmParams& p) {
   using L = GemmSmem<BN, kPair>;
@@ -171,9 +175,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint64_t* done = bars + 2 * kStages + 4;
-  uint64_t* ringbar = bars + 2 * kStages + 5;  // per-column scale slots filled
+  uint64_t* sfull = bars + 2 * kStages + 5;  // scale slot landed (32 producer lanes)
+  uint64_t* sempty = sfull + L::kScaleSlots;  // scale slot read (8 promotion warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
-  float* ring = reinterpret_cast<float*>(smem + L::kRingOff);
+  float* scales = reinterpret_cast<float*>(smem + L::kScaleOff);
+  constexpr int kSlots = L::kScaleSlots, kSlotFloats = L::kScaleSlotFloats;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: this CTA issues the MMAs
@@ -190,8 +196,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_init(&tempty[b], kPair ? 16 : 8);  // one arrival per promotion warp (of both CTAs)
     }
     mbar_init(done, 1);
-    mbar_init(&ringbar[0], 256);
-    mbar_init(&ringbar[1], 256);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sfull[i], 32);
+      mbar_init(&sempty[i], 8);
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -219,23 +227,48 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     setmaxnreg_dec<kSmallRegs>();
     if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int u = unit0; u < p.units && ok; u += unit_step) {
-        UnitCoords c = unit_coords(p, u);
-        for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
-          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, 0x301u)) {
-            ok = false;
-            break;
+    // Lane 0 issues the operand tiles (TMA); every lane copies its share of
+    // the slice's scales into the scale ring (cp.async, completion counted
+    // on the slot's barrier), so the promotion warps never wait on global
+    // memory for a scale.
+    const int nkb = p.K / 128;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = unit0; u < p.units && ok; u += unit_step) {
+      UnitCoords c = unit_coords(p, u);
+      const int m_rows = c.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
+      for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+        const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+        const uint32_t q = it % kSlots, qph = (it / kSlots) & 1u;
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(&empty[s], ph ^ 1u, p.wait_ns, 0x301u);
+        w_ok = mbar_wait(&sempty[q], qph ^ 1u, p.wait_ns, 0x303u) && w_ok;
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        float* slot = scales + q * kSlotFloats;
+        cp_async16(slot + 4 * lane, p.sa + static_cast<int64_t>(kb) * p.M + m_rows + 4 * lane);
+        if constexpr (SBMODE == kSbCol) {
+#pragma unroll
+          for (int r = 0; r < BN / 128; ++r)
+            cp_async16(slot + 128 + 128 * r + 4 * lane,
+                       p.sb + static_cast<int64_t>(kb) * p.N + c.nt * BN + 128 * r + 4 * lane);
+        } else {
+          if (lane < BN / 128) {
+            const int nb = c.nt * (BN / 128) + lane;  // column block
+            const float* src = SBMODE == kSbBlock ? p.sb + static_cast<int64_t>(nb) * nkb + kb
+                                                  : p.sb + static_cast<int64_t>(kb) * (p.N / 128) + nb;
+            cp_async4(slot + 128 + lane, src);
           }
+        }
+        cp_async_arrive(&sfull[q]);
+        if (lane == 0) {
           if constexpr (kPair) {
             // both CTAs' copies are counted on the first CTA's full[s]
             const uint32_t leader_full = mapa_shared(&full[s], 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (L::kABytes + L::kBBytes));
-            tma_load_2d_pair(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, c.m0 + 128 * static_cast<int>(rank),
-                             leader_full);
+            tma_load_2d_pair(smem + L::kAOff + s * L::kABytes, &tmA, kb * 128, m_rows, leader_full);
             tma_load_2d_pair(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128,
                              c.nt * BN + (BN / 2) * static_cast<int>(rank), leader_full);
           } else {
@@ -244,16 +277,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             tma_load_2d(smem + L::kBOff + s * L::kBBytes, &tmB, kb * 128, c.nt * BN, &full[s]);
           }
         }
+        __syncwarp();
       }
-      // Do not leave while copies into this CTA's shared memory are in flight:
-      // wait for the last fill of every stage to land (for a pair, the first
-      // CTA's full barriers count both CTAs' copies; the second CTA is held
-      // by the cluster barrier at the end until the first is done).
-      if (!kPair || rank == 0) {
-        for (uint32_t j = 0; j < kStages && j < it; ++j) {
-          const uint32_t f = it - 1 - j;
-          mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
-        }
+    }
+    // Do not leave while copies into this CTA's shared memory are in flight:
+    // this lane's scale copies, and the last fill of every operand stage (for
+    // a pair, the first CTA's full barriers count both CTAs' copies; the
+    // second CTA is held by the cluster barrier at the end until the first
+    // is done).
+    cp_async_wait_all();
+    if (lane == 0 && (!kPair || rank == 0)) {
+      for (uint32_t j = 0; j < kStages && j < it; ++j) {
+        const uint32_t f = it - 1 - j;
+        mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
       }
     }
     } else if (warp == kMmaWarp) {
@@ -306,7 +342,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;  // tile row == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int nkb = p.K / 128;
     uint32_t it = 0;
     bool ok = true;
     float acc[kCols];
@@ -321,72 +356,29 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 #pragma unroll
       for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
 
-      // Scale pointers for this unit, advanced one slice at a time:
-      //   sa      [K/128, M]  -> this thread's row, stride M per slice
-      //   sb mode kSbBlock  [N/128, K/128] -> this thread's column block, stride 1
-      //   sb mode kSbBlockT [K/128, N/128] -> stride N/128
-      //   sb mode kSbCol    [K/128, N]     -> thread t's column (ring fill), stride N
-      const float* sa_ptr = p.sa + static_cast<int64_t>(c.kb0) * p.M + gm;
-      const float* sb_ptr;
-      int64_t sb_stride;
-      if constexpr (SBMODE == kSbBlock) {
-        sb_ptr = p.sb + static_cast<int64_t>(col0 / 128) * nkb + c.kb0;
-        sb_stride = 1;
-      } else if constexpr (SBMODE == kSbBlockT) {
-        sb_ptr = p.sb + static_cast<int64_t>(c.kb0) * (p.N / 128) + col0 / 128;
-        sb_stride = p.N / 128;
-      } else {
-        sb_ptr = p.sb + static_cast<int64_t>(c.kb0) * p.N + c.nt * BN + threadIdx.x;
-        sb_stride = p.N;
-      }
-      const bool col_loader = (BN == 256) || (threadIdx.x < BN);
-      float sa_next = __ldg(sa_ptr);
-      float sb_next = 0.0f;
-      if constexpr (SBMODE != kSbCol) {
-        sb_next = __ldg(sb_ptr);
-      } else {
-        // Slot it&1 holds the column scales of slice `it`; every promotion
-        // thread writes (at most) one value and arrives, readers wait for all 256.
-        if (col_loader) ring[(it & 1u) * BN + threadIdx.x] = __ldg(sb_ptr);
-        mbar_arrive(&ringbar[it & 1u]);
-      }
-
       for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
         const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-        const float sa_cur = sa_next;
-        const float sb_cur = sb_next;
-        float col_next = 0.0f;
-        if (kb + 1 < c.kb1) {
-          sa_ptr += p.M;
-          sb_ptr += sb_stride;
-          sa_next = __ldg(sa_ptr);
-          if constexpr (SBMODE != kSbCol) {
-            sb_next = __ldg(sb_ptr);
-          } else {
-            if (col_loader) col_next = __ldg(sb_ptr);
-          }
-        }
-        if constexpr (SBMODE == kSbCol) {
-          if (!mbar_wait(&ringbar[b], bph, p.wait_ns, 0x322u)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!mbar_wait(&tfull[b], bph, p.wait_ns, 0x321u)) {
+        const uint32_t q = it % kSlots, qph = (it / kSlots) & 1u;
+        if (!mbar_wait(&sfull[q], qph, p.wait_ns, 0x322u) || !mbar_wait(&tfull[b], bph, p.wait_ns, 0x321u)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        // this slice's scales: sa of this thread's row; sb of its column
+        // block (block modes) or its columns (kSbCol)
+        const float* slot = scales + q * kSlotFloats;
+        const float sa_cur = slot[row];
+        const float sb_cur = SBMODE == kSbCol ? 1.0f : slot[128 + (BN == 256 ? half : 0)];
+        const float* sbc = slot + 128 + half * kCols;
         const uint32_t taddr = tmem_base + lane_base + b * BN + half * kCols;
         // acc[j] += P[j] * scale(j) over this thread's kCols columns, read
         // from TMEM 64 columns at a time: each tcgen05.ld round trip is
         // long next to the FMAs it feeds, and tcgen05.wait::ld drains every
         // outstanding load, so fewer, wider loads shorten the chain.  The
         // buffer is released as soon as its last chunk is in registers.
-        const float s = sa_cur * sb_cur;
-        const float2 s2 = make_float2(s, s);
+        const float sc = sa_cur * sb_cur;
+        const float2 s2 = make_float2(sc, sc);
         const float2 sa2 = make_float2(sa_cur, sa_cur);
-        const float* sbc = ring + b * BN + half * kCols;
 #pragma unroll
         for (int ch = 0; ch < kCols / 64; ++ch) {
           uint32_t v[64];
@@ -407,19 +399,51 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                             sbc + ch * 64 + 32);
           reg_fence64(acc + ch * 64);
         }
-        if constexpr (SBMODE == kSbCol) {
-          // Everyone has passed this slice's ring wait, so every thread is
-          // done with slot (it+1)&1 (last read for slice it-1): refill it.
-          if (kb + 1 < c.kb1) {
-            if (col_loader) ring[((it + 1) & 1u) * BN + threadIdx.x] = col_next;
-            mbar_arrive(&ringbar[(it + 1) & 1u]);
-          }
-        }
+        // the slot's scales have been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[q]);
       }
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if (p.splits == 1 && p.Cq == nullptr) {
+      if constexpr (kFused) {
+        // One split, BN = 256, codes requested: bf16 and E4M3 outputs are
+        // stored directly (each thread owns whole 128-column groups).
+        // bf16 output, 8 columns (16 bytes) per store.
+        uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.N + col0;
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kCols / 8; ++i) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+          }
+          *reinterpret_cast<uint4*>(crow + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        {
+          // E4M3 codes of the bf16 values of this thread's 128-column group,
+          // with the activation quantiser's rule (m is their amax).
+          const GroupScale g = make_group_scale(m);
+          uint8_t* qrow = p.Cq + static_cast<int64_t>(gm) * p.N + col0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = 16 * i + 4 * j;
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c], acc[c + 1]);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
+              const uint32_t l = *reinterpret_cast<const uint32_t*>(&lo), h = *reinterpret_cast<const uint32_t*>(&hi);
+              w[j] = quant_pair(bf16lo(l), bf16hi(l), g) | (quant_pair(bf16lo(h), bf16hi(h), g) << 16);
+            }
+            *reinterpret_cast<uint4*>(qrow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = g.s;
+        }
+      } else if (p.splits == 1) {
         // bf16 output through shared memory and TMA stores: this warp's 32
         // rows x kCols columns go to its staging boxes (64 columns, 128-byte
         // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), then lane
@@ -444,43 +468,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 #pragma unroll
           for (int bx = 0; bx < kCols / 64; ++bx) tma_store_2d(&tmC, stg + bx * 4096, col0 + 64 * bx, c.m0 + quad * 32);
           bulk_commit_group();
-        }
-      } else if (p.splits == 1) {
-        // bf16 output, 8 columns (16 bytes) per store.
-        uint16_t* crow = p.C + static_cast<int64_t>(gm) * p.N + col0;
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kCols / 8; ++i) {
-          uint32_t w[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[8 * i + 2 * j], acc[8 * i + 2 * j + 1]);
-            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-            m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
-          }
-          *reinterpret_cast<uint4*>(crow + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        if constexpr (BN == 256) {
-          if (p.Cq != nullptr) {
-          // E4M3 codes of the bf16 values of this thread's 128-column group,
-          // with the activation quantiser's rule (m is their amax).
-          const GroupScale g = make_group_scale(m);
-          uint8_t* qrow = p.Cq + static_cast<int64_t>(gm) * p.N + col0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = 16 * i + 4 * j;
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[c], acc[c + 1]);
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
-              const uint32_t l = *reinterpret_cast<const uint32_t*>(&lo), h = *reinterpret_cast<const uint32_t*>(&hi);
-              w[j] = quant_pair(bf16lo(l), bf16hi(l), g) | (quant_pair(bf16lo(h), bf16hi(h), g) << 16);
-            }
-            *reinterpret_cast<uint4*>(qrow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = g.s;
-          }
         }
       } else {
         float* prow = p.Cpart + (static_cast<int64_t>(c.split) * p.M + gm) * p.N + col0;
@@ -507,19 +494,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
-template <int BN, int SBMODE>
+// kFused selects the instance with the quantised (E4M3) epilogue.  It is a
+// separate instance so that the plain GEMM holds no division code: the
+// fused epilogue's IEEE division fallbacks would otherwise sit (unused) in
+// every GEMM kernel and take part in its register allocation.
+template <int BN, int SBMODE, bool kFused = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  gemm_body<BN, SBMODE, false>(tmA, tmB, tmC, p);
+  static_assert(!kFused || BN == 256, "the fused epilogue needs whole 128-column groups per thread");
+  gemm_body<BN, SBMODE, false, kFused>(tmA, tmB, tmC, p);
 }
 
 // 256 x 256 output tiles on CTA pairs (clusters of two).
-template <int SBMODE>
+template <int SBMODE, bool kFused = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     block_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  gemm_body<256, SBMODE, true>(tmA, tmB, tmC, p);
+  gemm_body<256, SBMODE, true, kFused>(tmA, tmB, tmC, p);
 }
 
 // Adds the fp32 split-K partials in split order, rounds to bf16 and,

@@ -12,29 +12,35 @@
 //
 // Work decomposition.  The input is cut into 128x128 bf16 tiles (32 KB),
 // walked in row-major order by a persistent grid (two CTAs per SM).  A CTA
-// streams its tiles through a 3-deep shared-memory ring filled by bulk
-// copies; its eight warps share each tile without any block-wide barrier
-// (warp 0 also refills a slot once every warp has released it).  Warp w owns
-//   * rows 16w..16w+15 (their 1x128 groups along the columns: q, s): lane
-//     pair (2j, 2j+1) holds row 16w+j, 64 values each, as the 16-code output
-//     chunks 2m+h (h = lane & 1), and
-//   * columns 16w..16w+15 (their groups of 128 rows: qT, sT): lane l holds
-//     columns 16w+4(l%4)..+3 over rows 16(l/4)..16(l/4)+15.
+// streams its tiles through a 3-deep shared-memory ring filled by TMA; its
+// eight warps share each tile without any block-wide barrier (warp 0 also
+// refills a slot once every warp has released it).  Warp w owns
+//   * 16 rows of the tile (their 1x128 groups along the columns: q, s):
+//     lane pair (2j, 2j+1) holds one row, 64 values each, as the 16-code
+//     output chunks 2m+h (h = lane & 1), and
+//   * columns 16w..16w+15 (their groups of 128 rows: qT, sT): each lane holds
+//     4 columns over 16 consecutive rows.
 // It copies both slices into registers, releases the ring slot, reduces
 // amaxes with in-lane packed bf16 maxima and a few shuffles, turns each
-// amax into its scale and reciprocal once per warp instruction stream, forms
-// every code from the correctly rounded quotient (GroupScale), and stores codes
-// straight to global memory in 32-byte (rows) and 128-byte (columns)
-// segments.  The input is read from HBM once whichever outputs are requested.
+// amax into its scale and reciprocal once, forms every code from the
+// correctly rounded quotient (GroupScale), and stores codes straight to
+// global memory in 32-byte (rows) and 128-byte (columns) segments.  The
+// input is read from HBM once whichever outputs are requested.
 //
-// Shared-memory image of a tile: row r (256 bytes) starts at byte
-// 272 r + 32 ((r / 16) % 8).  The 16-byte stride padding and the per-block
-// offset make both register views conflict-free: in the row view 16
-// consecutive rows cover the eight 16-byte bank groups twice per half-warp;
-// in the column view rows 16 apart start 32 bytes (8 banks) apart, so eight
-// of them tile the 32 banks in two wavefronts, the minimum for 256 bytes.
+// Shared-memory image of a tile.  The input is addressed by TMA as the 2-D
+// tensor [R/16, 16 C]: its row y holds rows 16y..16y+15 of the input side by
+// side, so a 64-column x 8-row box at x = l C + c0 + 64h, y = r0/16 fetches
+// rows r0 + l, r0 + 16 + l, ..., r0 + 112 + l.  Thirty-two such boxes
+// (l = 0..15, h = 0..1), 128-byte swizzled, place element (r, c) of the tile,
+// r = 16 a + l, c = 64 h + 8 k + e, at byte
+//   16384 h + 1024 l + 128 a + 16 (k XOR a) + 2 e.
+// Rows 16 apart therefore sit in different swizzle phases, and the lane
+// assignments below make both register views conflict-free: a quarter-warp
+// of 16-byte row reads covers rows of four distinct a (0,1,4,5 or 2,3,6,7),
+// and a half-warp of 8-byte column reads covers row blocks of one parity.
 #pragma once
 
+#include <cuda.h>
 #include "common.cuh"
 
 namespace bfp8 {
@@ -47,19 +53,34 @@ struct QuantParams {
   uint8_t* qT;  // [C, R] or null
   float* sT;    // act: [R/128, C];  unused for weights
   uint64_t wait_ns;
+  uint32_t ctiles, tiles;  // C/128 and (R/128)(C/128), filled in by the launcher
 };
+
+// Which outputs a kernel instance writes (a template bit set).
+constexpr int kQRows = 1;  // q, s: groups along the columns (or the block, rows view)
+constexpr int kQCols = 2;  // qT (, sT): groups along the rows, stored transposed
 
 constexpr int kQComputeWarps = 8;
 constexpr int kQuantThreads = 32 * kQComputeWarps;
 constexpr int kQStages = 3;
-constexpr int kQTileBytes = 128 * 256;                     // bf16 payload of a tile
-constexpr int kQBufBytes = 35072;                          // padded image, >= 272*127 + 32*7 + 256
-constexpr int kQBarOff = kQStages * kQBufBytes;            // full[3], empty[3], redbar[2]
+constexpr int kQTileBytes = 128 * 256;                       // bf16 tile, also the ring slot
+constexpr int kQBarOff = kQStages * kQTileBytes;             // full[3], empty[3], redbar[2]
 constexpr int kQRedOff = kQBarOff + (2 * kQStages + 2) * 8;  // float[2][8] (weight block amax)
-constexpr int kQuantSmemBytes = kQRedOff + 2 * kQComputeWarps * 4;
-static_assert(272 * 127 + 32 * 7 + 256 <= kQBufBytes, "tile image overflows its buffer");
+constexpr int kQuantSmemBytes = kQRedOff + 2 * kQComputeWarps * 4 + 1024;  // + room to align to 1024
 
-__device__ __forceinline__ uint32_t qrow_off(int r) { return 272u * r + 32u * ((r >> 4) & 7); }
+// Tile coordinates of a persistent CTA's walk (tile t = rt * ctiles + ct).
+struct TileWalk {
+  uint32_t t, rt, ct;
+  __device__ __forceinline__ void advance(uint32_t step, uint32_t drt, uint32_t dct, uint32_t ctiles) {
+    t += step;
+    rt += drt;
+    ct += dct;
+    if (ct >= ctiles) {
+      ct -= ctiles;
+      ++rt;
+    }
+  }
+};
 
 __device__ __forceinline__ float bf16x2_absmax(uint32_t w) { return fmaxf(fabsf(bf16lo(w)), fabsf(bf16hi(w))); }
 
@@ -73,7 +94,7 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
 
 // 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i),
 // one group.  Groups with extreme scales (g.exact false) take the IEEE
-// division; the branch is uniform over the group.
+// division.
 __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
   if (g.exact) {
     const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
@@ -86,10 +107,18 @@ __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupSca
   return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
+// The same on the FMA path only (every group of the tile has g.exact).
+__device__ __forceinline__ uint4 quant16w_fast(const uint32_t (&w)[8], const GroupScale& g) {
+  const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
+  return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
+                    quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
+}
+
 // 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
+template <bool kFast>
 __device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  return quant16w(w, g);
+  return kFast ? quant16w_fast(w, g) : quant16w(w, g);
 }
 
 // Values k and k+1 of one column (element kHalf of word kWord of row slices
@@ -101,39 +130,68 @@ __device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
 }
 
 // 16 codes of one column over 16 rows, one group.  Codes in row order.
-template <int kWord, int kHalf>
+template <int kWord, int kHalf, bool kFast>
 __device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupScale& g) {
   uint32_t w[8];
 #pragma unroll
   for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
-  return quant16w(w, g);
+  return kFast ? quant16w_fast(w, g) : quant16w(w, g);
 }
 
-// kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
-// kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
-// Issues the bulk copies of tile t into ring slot `buf` (one whole warp;
-// lane 0 arms the slot's barrier).
-__device__ __forceinline__ void quant_fill(const QuantParams& p, int64_t t, int64_t ctiles, uint8_t* buf,
+// Whether a scale lies in the range where the FMA path is exact (the range
+// make_group_scale tests).
+__device__ __forceinline__ bool scale_on_fma_path(float s) { return s >= 0x1p-80f && s <= 0x1p+100f; }
+
+// Warp 0 fetches tile (rt, ct) into ring slot `buf` with 32 TMA boxes (one
+// per lane; lane 0 arms the slot's barrier first).
+__device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t C, uint32_t rt, uint32_t ct, uint8_t* buf,
                                            uint64_t* bar, int lane) {
-  const int64_t r0 = (t / ctiles) * 128, c0 = (t % ctiles) * 128;
   if (lane == 0) mbar_arrive_expect_tx(bar, kQTileBytes);
   __syncwarp();
-  for (int r = lane; r < 128; r += 32) bulk_g2s(buf + qrow_off(r), p.x + (r0 + r) * p.C + c0, 256, bar);
+  const int l = lane >> 1, h = lane & 1;
+  tma_load_2d(buf + 16384 * h + 1024 * l, tmx, static_cast<int32_t>(l * C + ct * 128 + 64 * h),
+              static_cast<int32_t>(rt * 8), bar);
+}
+
+// Codes of this warp's row and column slices of one tile, stored to global
+// memory.  kFast: every group scale of the warp is on the FMA path, so the
+// whole body is one branch-free block the compiler can interleave.
+template <int kMode, bool kFast>
+__device__ __forceinline__ void quant_tile_codes(const uint4 (&rv)[8], const uint2 (&cv)[16], const GroupScale& grow,
+                                                 const GroupScale (&gc)[4], uint8_t* qrow, uint8_t* qcol,
+                                                 int64_t R) {
+  if constexpr ((kMode & kQRows) != 0) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast>(rv[2 * m], rv[2 * m + 1], grow);
+  }
+  if constexpr ((kMode & kQCols) != 0) {
+    GroupScale g[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_on_fma_path(gc[k].s)};
+    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast>(cv, g[0]);
+    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast>(cv, g[1]);
+    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast>(cv, g[2]);
+    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast>(cv, g[3]);
+  }
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
 // kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
-template <bool kWeight>
-__global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const QuantParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+template <bool kWeight, int kMode>
+__global__ void __launch_bounds__(kQuantThreads, 2)
+    quantize_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
+  constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQBarOff);
   uint64_t* empty = full + kQStages;
   uint64_t* redbar = empty + kQStages;  // weight block amax exchange, by tile parity
   float* red = reinterpret_cast<float*>(smem + kQRedOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ctiles = p.C / 128;
-  const int64_t tiles = (p.R / 128) * ctiles;
+  const uint32_t ctiles = p.ctiles, tiles = p.tiles, C = static_cast<uint32_t>(p.C);
+  const uint32_t step = gridDim.x, drt = step / ctiles, dct = step % ctiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
@@ -145,63 +203,73 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
     fence_mbar_init();
   }
   __syncthreads();
-  // prologue: warp 0 issues the first kQStages tiles of this CTA, and later
-  // each tile j-1+kQStages at iteration j.
-  int64_t last_issued = -1;  // latest tile (local index) this warp issued after the prologue
-  uint32_t prologue = 0;     // tiles issued by the prologue (warp 0)
+
+  TileWalk cur{blockIdx.x, blockIdx.x / ctiles, blockIdx.x % ctiles};
+  // Warp 0 issues the first kQStages tiles of this CTA, and later (at
+  // iteration j) tile j-1+kQStages into the slot tile j-1 used.
+  TileWalk fill = cur;
+  uint32_t issued = 0;  // tiles of this CTA issued so far (warp 0)
   if (warp == 0) {
-    int64_t t = blockIdx.x;
-    for (; prologue < kQStages && t < tiles; ++prologue, t += gridDim.x)
-      quant_fill(p, t, ctiles, smem + prologue * kQBufBytes, &full[prologue], lane);
+    for (; issued < kQStages && fill.t < tiles; ++issued) {
+      quant_fill(&tmx, C, fill.rt, fill.ct, smem + issued * kQTileBytes, &full[issued], lane);
+      fill.advance(step, drt, dct, ctiles);
+    }
   }
 
-  const bool rows = p.q != nullptr, cols = p.qT != nullptr;
-  const int rj = lane >> 1, rh = lane & 1;   // row view: row 16w + rj, chunks 2m + rh
-  const int cq = lane & 3, rg = lane >> 2;   // column view: columns 16w + 4cq.., rows 16rg..
-  const int wrow = 16 * warp + rj;
+  // Row view: lane pair (2j, 2j+1) holds tile row 16 a + l with
+  // a = j%8 with its bits 1 and 2 swapped, l = 2w + j/8; lane h = lane & 1
+  // reads 16-byte chunks 4m + 2h + u (u = 0, 1) of it.
+  const int jj = lane >> 1, hh = lane & 1;
+  const int ra = (jj & 1) | (((jj >> 2) & 1) << 1) | (((jj >> 1) & 1) << 2);
+  const int wrow = 16 * ra + 2 * warp + (jj >> 3);
+  // chunk 2h of the row; chunk 4(m%2) + 2h + u differs from it in the bits
+  // 4(m%2) + u of the 16-byte index, which the swizzle XOR leaves alone
+  const uint32_t roff = 1024u * (2 * warp + (jj >> 3)) + 128u * ra + ((static_cast<uint32_t>(2 * hh) ^ ra) << 4);
+  // Column view: lane (cq, g) holds columns 16w + 4cq..+3 over rows
+  // 16 rg..16 rg + 15, rg = 2 (g % 4) + g / 4.
+  const int cq = lane & 3, g = lane >> 2, rg = 2 * (g & 3) + (g >> 2);
+  const uint32_t coff = 16384u * (warp >> 2) + 128u * rg +
+                        ((static_cast<uint32_t>(2 * (warp & 3) + (cq >> 1)) ^ rg) << 4) + 8u * (cq & 1);
+
   uint32_t j = 0;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+  for (; cur.t < tiles; cur.advance(step, drt, dct, ctiles), ++j) {
     const uint32_t s = j % kQStages, ph = (j / kQStages) & 1u;
     if (!mbar_wait(&full[s], ph, p.wait_ns, kWeight ? 0x201u : 0x101u)) break;
-    const uint8_t* buf = smem + s * kQBufBytes;
-    const int64_t r0 = (t / ctiles) * 128, c0 = (t % ctiles) * 128;
+    const uint8_t* buf = smem + s * kQTileBytes;
+    const int64_t r0 = static_cast<int64_t>(cur.rt) * 128, c0 = static_cast<int64_t>(cur.ct) * 128;
 
     // both slices into registers, then hand the slot back
     uint4 rv[8];
     uint2 cv[16];
-    if (rows) {
-      const uint8_t* rp = buf + qrow_off(wrow);
+    if constexpr (kRows) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        rv[2 * m] = *reinterpret_cast<const uint4*>(rp + (2 * (2 * m + rh)) * 16);
-        rv[2 * m + 1] = *reinterpret_cast<const uint4*>(rp + (2 * (2 * m + rh) + 1) * 16);
+        rv[2 * m] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1))));
+        rv[2 * m + 1] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1) + 16u)));
       }
     }
-    if (cols) {
+    if constexpr (kCols) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        cv[k] = *reinterpret_cast<const uint2*>(buf + qrow_off(16 * rg + k) + 32 * warp + 8 * cq);
+      for (int k = 0; k < 16; ++k) cv[k] = *reinterpret_cast<const uint2*>(buf + coff + 1024 * k);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (warp == 0 && j >= 1) {
+    if (warp == 0 && j >= 1 && fill.t < tiles) {
       // Refill the slot of tile j-1 (every warp released it, usually long
       // ago) with tile j-1+kQStages.
-      const int64_t tn = t + (kQStages - 1) * static_cast<int64_t>(gridDim.x);
-      if (tn < tiles) {
-        const uint32_t f = j - 1, sf = f % kQStages;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        quant_fill(p, tn, ctiles, smem + sf * kQBufBytes, &full[sf], lane);
-        last_issued = f + kQStages;
-      }
+      const uint32_t f = j - 1, sf = f % kQStages;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      quant_fill(&tmx, C, fill.rt, fill.ct, smem + sf * kQTileBytes, &full[sf], lane);
+      fill.advance(step, drt, dct, ctiles);
+      ++issued;
     }
 
     // amaxes (packed bf16, NaN ignored)
     float row_m = 0.0f;
     uint32_t m01 = 0u, m23 = 0u;
-    if (rows) {
+    if constexpr (kRows) {
       uint32_t m2 = 0u;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -209,7 +277,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
       row_m = bf16x2_absmax(m2);
       row_m = fmaxf(row_m, __shfl_xor_sync(0xffffffffu, row_m, 1));
     }
-    if (cols) {
+    if constexpr (kCols) {
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         m01 = bf16x2_maxabs(m01, cv[k].x);
@@ -222,12 +290,13 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
       }
     }
 
-    GroupScale grow, gcol;  // this lane's row group; column 4cq + rg%4 (scales of the other columns by shuffle)
+    GroupScale grow, gc[4];  // this lane's row group; its 4 columns' groups
+    bool all_exact;
     if constexpr (kWeight) {
       // one block: every warp's maxima meet in shared memory.  Slot j%2 is
       // reused two tiles later, when every warp has read it (a warp arrives
       // for tile j+1 only after reading slot j%2).
-      float m = rows ? row_m : fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23));
+      float m = kRows ? row_m : fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23));
       m = warp_max(m);
       float* rbuf = red + (j & 1u) * kQComputeWarps;
       if (lane == 0) {
@@ -239,47 +308,42 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
 #pragma unroll
       for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
       grow = make_group_scale(bm);
-      gcol = grow;
-      if (threadIdx.x == 0) p.s[(r0 / 128) * (p.C / 128) + c0 / 128] = grow.s;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) gc[k] = grow;
+      all_exact = grow.exact;  // uniform over the block
+      if (threadIdx.x == 0) p.s[cur.rt * static_cast<int64_t>(ctiles) + cur.ct] = grow.s;
     } else {
-      if (rows) {
+      bool ok = true;
+      if constexpr (kRows) {
         grow = make_group_scale(row_m);
-        if (rh == 0) p.s[(c0 / 128) * p.R + r0 + wrow] = grow.s;
+        ok = grow.exact;
+        if (hh == 0) p.s[static_cast<int64_t>(cur.ct) * p.R + r0 + wrow] = grow.s;
       }
-      if (cols) {
-        const int sel = rg & 3;
+      if constexpr (kCols) {
+        // lane (cq, g) forms the scale of column 4cq + g%4; lanes cq + 4k
+        // hold those of this lane's columns
+        const int sel = g & 3;
         const uint32_t mw = sel < 2 ? m01 : m23;
-        gcol = make_group_scale(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
-        if (rg < 4) p.sT[(r0 / 128) * p.C + c0 + 16 * warp + 4 * cq + rg] = gcol.s;
+        const GroupScale gcol = make_group_scale(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
+        ok = ok && gcol.exact;
+        if (g < 4) p.sT[static_cast<int64_t>(cur.rt) * p.C + c0 + 16 * warp + 4 * cq + g] = gcol.s;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          gc[k].s = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
+          gc[k].r = __shfl_sync(0xffffffffu, gcol.r, cq + 4 * k);
+          gc[k].exact = true;  // restated from s on the slow path
+        }
       }
+      all_exact = __all_sync(0xffffffffu, ok);
     }
 
     // codes
-    if (rows) {
-      uint8_t* qrow = p.q + (r0 + wrow) * p.C + c0;
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<uint4*>(qrow + (2 * m + rh) * 16) = quant16(rv[2 * m], rv[2 * m + 1], grow);
-    }
-    if (cols) {
-      // the scales of this lane's 4 columns live in lanes cq + 4k
-      GroupScale gc[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if constexpr (kWeight) {
-          gc[k] = gcol;
-        } else {
-          gc[k].s = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
-          gc[k].r = __shfl_sync(0xffffffffu, gcol.r, cq + 4 * k);
-          gc[k].exact = __shfl_sync(0xffffffffu, gcol.exact, cq + 4 * k);
-        }
-      }
-      uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
-      *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0>(cv, gc[0]);
-      *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1>(cv, gc[1]);
-      *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0>(cv, gc[2]);
-      *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1>(cv, gc[3]);
-    }
+    uint8_t* qrow = kRows ? p.q + (r0 + wrow) * p.C + c0 + 16 * hh : nullptr;
+    uint8_t* qcol = kCols ? p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg : nullptr;
+    if (all_exact)
+      quant_tile_codes<kMode, true>(rv, cv, grow, gc, qrow, qcol, p.R);
+    else
+      quant_tile_codes<kMode, false>(rv, cv, grow, gc, qrow, qcol, p.R);
   }
   // Leave no copy in flight into this CTA's shared memory: after an early
   // exit at local tile j, warp 0 (which issues every copy) waits (bounded)
@@ -288,8 +352,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quantize_tile_kernel(const Q
   // the tile), so the waited phase is the one of that tile.  After a normal
   // exit j counts all tiles of the CTA and nothing is waited for.
   if (warp == 0 && lane == 0) {
-    const int64_t last = last_issued > static_cast<int64_t>(prologue) - 1 ? last_issued : static_cast<int64_t>(prologue) - 1;
-    for (int64_t k = j; k <= last; ++k)
+    for (uint32_t k = j; k < issued; ++k)
       mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, p.wait_ns, kWeight ? 0x212u : 0x112u);
   }
 }
