@@ -22,6 +22,14 @@ Readings where the pages are silent: the scale is an arbitrary fp32 value
 amax/448 (not the power of two used on SM120); quantisation divides by s
 rather than multiplying by 448/amax; an all-zero group gets s = 1.
 
+Power-of-two mode (scale_mode="pow2").  Section 3.2 of the paper runs the
+same grouping on SM120 through the hardware MXFP8 path, whose scales are
+powers of two.  In this mode s is the smallest power of two with
+s >= amax/448, i.e. s = 2^ceil(log2(amax/448)), so no value of the group
+saturates and the largest lands in (224, 448]; an all-zero group keeps
+s = 1.  Step 3 is unchanged: x/s with s a power of two is an exact scaling
+(rounded once only where it leaves the fp32 range).
+
 Scale layouts (shared with the C ABI, which states the same contract):
 
 * quantize_act_1x128(X [R, C]) groups along C:  q [R, C],  s [C/128, R]
@@ -58,6 +66,35 @@ def group_scale(amax):
     return np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
 
 
+def group_scale_pow2(amax):
+    """Power-of-two scale of a group: the smallest 2^k >= amax/448 (1 when
+    amax == 0), as float32.
+
+    t = amax/448 is formed in float64.  For a float32 amax that quotient is
+    either exactly a power of two (amax = 7 * 2^j) or further than 2^-26 in
+    relative terms from every power of two (amax has at most 24 significant
+    bits, so amax/7 cannot come closer), far more than the 2^-53 rounding of
+    the float64 division; ceil(log2(t)) is therefore read off frexp exactly:
+    t = f * 2^e with f in [0.5, 1) gives k = e - 1 when f == 0.5, else e.
+    """
+    amax = np.asarray(amax, dtype=np.float32)
+    t = amax.astype(np.float64) / 448.0
+    f, e = np.frexp(t)
+    k = np.where(f == 0.5, e - 1, e)
+    s = np.ldexp(np.float64(1.0), k).astype(np.float32)  # 2^k for k in [-141, 120]: exact in float32
+    return np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+
+
+SCALE_MODES = {"amax448": group_scale, "pow2": group_scale_pow2}
+
+
+def _scale_fn(scale_mode):
+    try:
+        return SCALE_MODES[scale_mode]
+    except KeyError:
+        raise ValueError(f"unknown scale_mode {scale_mode!r}") from None
+
+
 def quantize_values(x, s):
     """q = E4M3(float32(x / s)), elementwise with broadcasting."""
     x = np.asarray(x, dtype=np.float32)
@@ -67,7 +104,7 @@ def quantize_values(x, s):
     return e4m3_encode(y)
 
 
-def quantize_act_1x128(x):
+def quantize_act_1x128(x, scale_mode="amax448"):
     """Quantise X [R, C] in 1x128 groups along C.
 
     Returns (q uint8 [R, C], s float32 [C/128, R]).
@@ -76,12 +113,12 @@ def quantize_act_1x128(x):
     R, C = x.shape
     xg = x.reshape(R, C // GROUP, GROUP)
     amax = np.nanmax(np.abs(xg), axis=2) if xg.size else np.zeros((R, C // GROUP), np.float32)
-    s = group_scale(amax)  # [R, C/128]
+    s = _scale_fn(scale_mode)(amax)  # [R, C/128]
     q = quantize_values(xg, s[:, :, None]).reshape(R, C)
     return q, np.ascontiguousarray(s.T)
 
 
-def quantize_act_tokens_1x128(x):
+def quantize_act_tokens_1x128(x, scale_mode="amax448"):
     """Quantise X [M, K] in groups of 128 consecutive rows (tokens) per column.
 
     This is the grouping that the weight-gradient GEMM needs, where the
@@ -89,10 +126,10 @@ def quantize_act_tokens_1x128(x):
     Returns (qT uint8 [K, M], sT float32 [M/128, K]).
     """
     x = _check_bf16_grid(x, "x")
-    return quantize_act_1x128(np.ascontiguousarray(x.T))
+    return quantize_act_1x128(np.ascontiguousarray(x.T), scale_mode)
 
 
-def quantize_w_128x128(w):
+def quantize_w_128x128(w, scale_mode="amax448"):
     """Quantise W [N, K] in 128x128 blocks.
 
     Returns (q uint8 [N, K], qT uint8 [K, N], s float32 [N/128, K/128]).
@@ -101,7 +138,7 @@ def quantize_w_128x128(w):
     N, K = w.shape
     wb = w.reshape(N // GROUP, GROUP, K // GROUP, GROUP)
     amax = np.nanmax(np.abs(wb), axis=(1, 3)) if wb.size else np.zeros((N // GROUP, K // GROUP), np.float32)
-    s = group_scale(amax)  # [N/128, K/128]
+    s = _scale_fn(scale_mode)(amax)  # [N/128, K/128]
     q = quantize_values(wb, s[:, None, :, None]).reshape(N, K)
     return q, np.ascontiguousarray(q.T), s
 

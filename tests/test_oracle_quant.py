@@ -4,7 +4,10 @@ Checked against: a hand-worked group (golden fixture), torch's float8 cast of
 a torch-computed x/s (library division and rounding), closed-form invariants
 of the amax/448 rule, the E4M3 round-trip error bound, group locality under
 single-element perturbations, and the paper's qualitative claim that local
-scales beat one scale per tensor when outliers are present.
+scales beat one scale per tensor when outliers are present.  The power-of-two
+mode is pinned by its own worked group, an exact-rational search for the
+scale over every positive bf16 amax, and torch's float8 cast of the exactly
+scaled values.
 """
 
 import numpy as np
@@ -172,3 +175,86 @@ def test_blockwise_beats_per_tensor_on_outliers(name):
     per = _rel_fro(x, T_DEC[qt] * float(st))
     assert blk < per
     assert blk < 0.05
+
+
+# ---------------------------------------------------------------- power of two
+
+
+def test_pow2_worked_example_group():
+    rows = read_golden("pow2_quant_worked_example.txt")
+    assert rows[0][0] == "scale"
+    want_s = float(rows[0][1])
+    x = np.zeros((1, 128), np.float32)
+    want = np.zeros(128, np.uint8)
+    for pos, xv, _xs, code in rows[1:]:
+        x[0, int(pos)] = np.float32(float(xv))
+        want[int(pos)] = int(code, 16)
+    assert np.array_equal(bf16_exact(x).view(np.uint32), x.view(np.uint32))
+    q, s = quant.quantize_act_1x128(np.tile(x, (128, 1)), scale_mode="pow2")
+    assert np.all(s == want_s)
+    assert np.array_equal(q[0], want) and np.array_equal(q[127], want)
+
+
+def _pow2_scale_by_search(amax):
+    """Smallest k with 2^k * 448 >= amax, by exact rational comparison."""
+    from fractions import Fraction
+    a = Fraction(float(amax))
+    k = 0
+    while Fraction(2) ** k * 448 < a:
+        k += 1
+    while Fraction(2) ** (k - 1) * 448 >= a:
+        k -= 1
+    return k
+
+
+def test_pow2_scale_of_every_bf16_amax():
+    bits = np.arange(1, 0x7F80, dtype=np.uint32) << 16  # every positive finite bf16 value
+    amax = bits.view(np.float32)
+    s = quant.group_scale_pow2(amax)
+    f, e = np.frexp(s.astype(np.float64))
+    assert np.all(f == 0.5)  # powers of two
+    for a, sv in zip(amax[::7], s[::7]):  # exact search on a stride through all binades
+        assert float(sv) == 2.0 ** _pow2_scale_by_search(a), a
+    # closed-form bounds on all of them: s >= amax/448 > s/2, in exact float64 products
+    a64, s64 = amax.astype(np.float64), s.astype(np.float64)
+    assert np.all(448.0 * s64 >= a64) and np.all(448.0 * s64 / 2 < a64)
+    assert quant.group_scale_pow2(np.float32(0.0)) == 1.0
+
+
+@pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_down", "x"), ("attn_proj", "x")])
+def test_pow2_codes_match_torch_cast_of_exact_scaling(name, tag):
+    wl = workloads.make(name)
+    x = workloads.tensor(wl, tag).float().numpy()[:256, :512]
+    q, s = quant.quantize_act_1x128(x, scale_mode="pow2")
+    xt = torch.from_numpy(x).view(256, 4, 128)
+    amax = xt.abs().amax(dim=2)
+    # independent scale: 2^ceil(log2(amax/448)) from torch's own frexp of the float64 quotient
+    mant, ex = torch.frexp(amax.double() / 448.0)
+    k = torch.where(mant == 0.5, ex - 1, ex)
+    st = torch.ldexp(torch.ones_like(amax, dtype=torch.float64), k).float()
+    assert np.array_equal(st.numpy(), s.T)
+    y = xt * (1.0 / st)[:, :, None]  # multiplying by 2^-k is exact here
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(256, 512).numpy()
+    assert np.array_equal(q, ref)
+    # nothing saturates: each group's amax/s lies in (224, 448] exactly, so its
+    # largest code decodes into [224, 448] (E4M3 rounding may reach 224)
+    ratio = amax.double().numpy() / st.double().numpy()
+    assert np.all((ratio > 224) & (ratio <= 448))
+    dec = T_DEC[q].reshape(256, 4, 128)
+    top = np.abs(dec).max(axis=2)
+    assert np.all((top >= 224) & (top <= 448))
+
+
+def test_pow2_weights_and_tokens_use_the_same_rule():
+    wl = workloads.make("tiny")
+    w = workloads.tensor(wl, "w").float().numpy()
+    q, qT, s = quant.quantize_w_128x128(w, scale_mode="pow2")
+    blk = np.abs(w.reshape(2, 128, 2, 128)).max(axis=(1, 3))
+    assert np.array_equal(s, quant.group_scale_pow2(blk))
+    assert np.array_equal(qT, q.T)
+    x = workloads.tensor(wl, "x").float().numpy()
+    qt, st = quant.quantize_act_tokens_1x128(x, scale_mode="pow2")
+    q2, s2 = quant.quantize_act_1x128(np.ascontiguousarray(x.T), scale_mode="pow2")
+    assert np.array_equal(qt, q2) and np.array_equal(st, s2)
+    with pytest.raises(ValueError):
+        quant.quantize_act_1x128(x, scale_mode="ue8m0")
