@@ -59,7 +59,246 @@ FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
 #   python bench.py --layers 1 --steps 1 --warmup 0 --no-e2e --no-cpu-baseline
 # Valid only for the kernel sources whose hash is the key; once the kernels
 # change the bench line reports null until a new capture is recorded.
-TRAFFIC = {"19c5bfe65fc0474b": {"gemm": 231.9e6, "quant": 155.1e6}}
+TRAFFIC = {
+    "19c5bfe65fc0474b": {"gemm": 231.9e6, "quant": 155.1e6},
+}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("common.cuh", "gemm.cuh", "quant.cuh", "api.cu"):
+        with open(os.path.join(ROOT, "blockwise_fp8_linear_quantise_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- host logic
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
+    ap.add_argument("--workload", default="stack28",
+                    choices=("tiny", "mlp_gateup", "mlp_down", "attn_proj", "stack28"))
+    ap.add_argument("--layers", type=int, default=28, help="stack28 only: layers to run (profiling cases)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=512)
+    ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--probe-fp8-peak", action="store_true",
+                    help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_group(world):
+    """A gloo group for the barrier and the max over ranks (host tensors
+    only: the replicas exchange no data)."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist.group.WORLD
+
+
+def barrier(group):
+    if group is not None:
+        import torch.distributed as dist
+        dist.barrier(group)
+
+
+def max_over_ranks(x, group):
+    if group is None:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def sum_over_ranks(x, group):
+    if group is None:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def linear_list(wl, layers):
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    specs = []
+    for s in wl.linears:
+        li = workloads.layer_of(s)
+        if li is None or li < layers:
+            specs.append(s)
+    return specs
+
+
+def gemm_flops(specs):
+    return sum(2 * s.M * s.N * s.K * (3 if s.backward else 1) for s in specs)
+
+
+def workload_config(wl, specs, layers):
+    cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M,
+           "shapes_MNK": sorted({(s.M, s.N, s.K) for s in specs}),
+           "passes": "fprop+dgrad+wgrad" if specs[0].backward else "fprop",
+           "l2": "inputs larger than L2: each step streams several GB through HBM (no explicit flush)",
+           "parallelism": "replicas (one independent step per GPU)"}
+    if wl.name == "stack28":
+        cfg["layers"] = layers
+        cfg["what"] = ("Puro-2B linear stack, one micro-step: per layer QKV 2048->4096, O 2048->2048, "
+                       "gate+up 2048->12288, down 6144->2048 on 16384 tokens; activations and output gradients "
+                       "N(0,1) with 0.1% x50 outliers, weights N(0,0.02^2), distinct per layer")
+    return cfg
+
+
+def summarise_clocks(rows):
+    """rows: parsed nvidia-smi samples -> the clocks object of the JSON line."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    sm = [r["sm"] for r in rows if r["sm"] is not None]
+    reasons = set()
+    for r in rows:
+        reasons.update(r["active"])
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(r["sm_max"] for r in rows if r["sm_max"] is not None) if sm else None,
+            "power_w_max": max((r["power"] for r in rows if r["power"] is not None), default=None),
+            "reasons": sorted(reasons), "samples": len(rows)}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons while the
+    timed region runs."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None or self.gpu_id is None:
+            return
+        self.proc = subprocess.Popen(
+            [exe, "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+             "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+    def stop(self):
+        if self.proc is None:
+            return summarise_clocks([])
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+
+            def num(v):
+                try:
+                    return float(v)
+                except ValueError:
+                    return None
+            rows.append({"sm": num(parts[0]), "sm_max": num(parts[1]), "power": num(parts[2]),
+                         "active": [n for n, v in zip(self.NAMES, parts[3:]) if v.lower() == "active"]})
+        return summarise_clocks(rows)
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_sample(wl, specs, tokens):
+    """CPU inputs for a bounded oracle sample: the first `tokens` tokens of
+    every distinct linear shape of the workload's first layer, drawn from the
+    workload's own distributions."""
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    seen, sample = set(), []
+    for s in specs:
+        key = (s.N, s.K, s.backward)
+        if key in seen:
+            continue
+        seen.add(key)
+        m = min(tokens, s.M)
+        f = lambda tag, shape: workloads.to_bf16(
+            workloads.draw(wl.dists[tag], shape, wl.seed, tag + "#cpu-sample")).float().numpy()
+        x = f(s.x_tag, (m, s.K))
+        w = f(s.w_tag, (s.N, s.K))
+        dy = f(s.dy_tag, (m, s.N)) if s.backward else None
+        sample.append((x, w, dy))
+    return sample
+
+
+def run_oracle(sample):
+    """Oracle linear forward (+ backward) over the sample; returns GEMM FLOPs."""
+    from oracle import gemm as ogemm
+    flops = 0
+    for x, w, dy in sample:
+        _, saved = ogemm.linear_fwd(x, w)
+        flops += 2 * x.shape[0] * w.shape[0] * x.shape[1]
+        if dy is not None:
+            ogemm.linear_bwd(dy, saved)
+            flops += 4 * x.shape[0] * w.shape[0] * x.shape[1]
+    return flops
+
+
+def describe_sample(sample):
+    return "; ".join(f"M={x.shape[0]} N={w.shape[0]} K={x.shape[1]} {'fwd+bwd' if dy is not None else 'fwd'}"
+                     for x, w, dy in sample)
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from blockwise_fp8_linear_quantise_b300 import workloads
+    wl = workloads.make(args.workload)
+    specs = linear_list(wl, args.layers)
+    sample = oracle_sample(wl, specs, args.ref_sample_tokens)
+    for _ in range(args.warmup):
+        run_oracle(sample)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += run_oracle(sample)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = cpu_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
+            "data": "synthetic", "config": workload_config(wl, specs, args.layers),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + describe_sample(sample)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
