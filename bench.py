@@ -86,6 +86,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--scale-mode", choices=["amax448", "pow2"], default="amax448",
+                    help="group scale rule: amax/448 (default) or the power-of-two mode")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
     return ap.parse_args(argv)
@@ -156,8 +158,8 @@ def gemm_flops(specs):
     return sum(2 * s.M * s.N * s.K * (3 if s.backward else 1) for s in specs)
 
 
-def workload_config(wl, specs, layers):
-    cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M,
+def workload_config(wl, specs, layers, scale_mode="amax448"):
+    cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M, "scale_mode": scale_mode,
            "shapes_MNK": sorted({(s.M, s.N, s.K) for s in specs}),
            "passes": "fprop+dgrad+wgrad" if specs[0].backward else "fprop",
            "l2": "inputs larger than L2: each step streams several GB through HBM (no explicit flush)",
@@ -295,7 +297,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
-            "data": "synthetic", "config": workload_config(wl, specs, args.layers),
+            "data": "synthetic", "config": workload_config(wl, specs, args.layers, args.scale_mode),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "per step: " + describe_sample(sample)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -313,12 +315,14 @@ class StackRunner:
     a step only makes the ctypes calls.
     """
 
-    def __init__(self, wl, specs, dev):
+    def __init__(self, wl, specs, dev, scale_mode="amax448"):
         import torch
         from blockwise_fp8_linear_quantise_b300 import _lib, ops, workloads
         self.torch = torch
         self.lib = _lib.load()
         self.ops = ops
+        self.scale_mode = scale_mode
+        self.mode_id = ops.SCALE_MODES[scale_mode]
         self.specs = specs
         self.dev = dev
         u8, f32, bf16 = torch.uint8, torch.float32, torch.bfloat16
@@ -373,18 +377,18 @@ class StackRunner:
             from blockwise_fp8_linear_quantise_b300 import workloads
             W = self.inputs[(s.w_tag, workloads.layer_of(s))]
             ne_w, ne_x = N * K, M * K
-            fwd.append(("quant_w", ne_w * (4 + 4 / 16384), lib.bfp8_quantize_w_128x128,
-                        (P(W), N, K, P(sc["Wq"]), P(sv["WqT"]), P(sv["sW"]))))
-            fwd.append(("quant_act", ne_x * (4 + 8 / 128), lib.bfp8_quantize_act_1x128,
-                        (P(X), M, K, P(sc["Xq"]), P(sc["sX"]), P(sv["XqT"]), P(sv["sXT"]))))
+            fwd.append(("quant_w", ne_w * (4 + 4 / 16384), lib.bfp8_quantize_w_128x128_ex,
+                        (P(W), N, K, P(sc["Wq"]), P(sv["WqT"]), P(sv["sW"]), self.mode_id)))
+            fwd.append(("quant_act", ne_x * (4 + 8 / 128), lib.bfp8_quantize_act_1x128_ex,
+                        (P(X), M, K, P(sc["Xq"]), P(sc["sX"]), P(sv["XqT"]), P(sv["sXT"]), self.mode_id)))
             fwd.append(("fprop", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
                         (self.ops.FPROP, P(sc["Xq"]), P(sc["sX"]), P(sc["Wq"]), P(sv["sW"]), M, N, K, P(sc["Y"]),
                          None, None, P(self.ws), self.ws_bytes)))
             if s.backward:
                 dY = self.inputs[(s.dy_tag, None)]
                 ne_y = M * N
-                b = [("quant_act", ne_y * (4 + 8 / 128), lib.bfp8_quantize_act_1x128,
-                      (P(dY), M, N, P(sc["dYq"]), P(sc["sdY"]), P(sc["dYqT"]), P(sc["sdYT"]))),
+                b = [("quant_act", ne_y * (4 + 8 / 128), lib.bfp8_quantize_act_1x128_ex,
+                      (P(dY), M, N, P(sc["dYq"]), P(sc["sdY"]), P(sc["dYqT"]), P(sc["sdYT"]), self.mode_id)),
                      ("dgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
                       (self.ops.DGRAD, P(sc["dYq"]), P(sc["sdY"]), P(sv["WqT"]), P(sv["sW"]), M, K, N, P(sc["dX"]),
                        None, None, P(self.ws), self.ws_bytes)),
@@ -463,7 +467,8 @@ class StackRunner:
             for ev in evs:
                 ms.wait_event(ev)
             Y = self.scratch[(s.M, s.N, s.K)]["Y"]
-            ops.linear_fwd(self.inputs[keys[0]], self.inputs[keys[1]], Y=Y, saved=self.saved[i], workspace=self.ws)
+            ops.linear_fwd(self.inputs[keys[0]], self.inputs[keys[1]], Y=Y, saved=self.saved[i], workspace=self.ws,
+                           scale_mode=self.scale_mode)
             if not s.backward:
                 done = torch.cuda.Event()
                 done.record(ms)
@@ -479,7 +484,8 @@ class StackRunner:
                 continue
             ms.wait_event(need((s.dy_tag, None)))
             dX = self.scratch[(s.M, s.N, s.K)]["dX"]
-            ops.linear_bwd(self.inputs[(s.dy_tag, None)], self.saved[i], dX=dX, dW=self.dW[i], workspace=self.ws)
+            ops.linear_bwd(self.inputs[(s.dy_tag, None)], self.saved[i], dX=dX, dW=self.dW[i], workspace=self.ws,
+                           scale_mode=self.scale_mode)
             done = torch.cuda.Event()
             done.record(ms)
             down.wait_event(done)
@@ -528,7 +534,7 @@ def gpu_arm(args):
     wl = workloads.make(args.workload)
     layers = args.layers if args.workload == "stack28" else 0
     specs = linear_list(wl, layers)
-    runner = StackRunner(wl, specs, dev)
+    runner = StackRunner(wl, specs, dev, args.scale_mode)
     flops_step = gemm_flops(specs)
 
     # warm-up
@@ -639,7 +645,7 @@ def gpu_arm(args):
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
-                "data": "synthetic", "config": workload_config(wl, specs, layers),
+                "data": "synthetic", "config": workload_config(wl, specs, layers, args.scale_mode),
                 "roofline": roofline, "roofline_quant": roofline_q, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk, "per_kernel": per_kernel,
                 "gemm_tflop_per_step": flops_step / 1e12, "kernel_source": src_hash}

@@ -68,18 +68,24 @@ bfp8_status device_state(DeviceState** out) {
     }
     cudaError_t e = cudaSuccess;
     // two quantiser CTAs per SM need the largest shared-memory carveout
-#define BFP8_SET_QUANT_SMEM(W, MODE)                                                                           \
+#define BFP8_SET_QUANT_SMEM(W, MODE, POW2)                                                                     \
   if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              kQuantSmemBytes);                                                                  \
   if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    BFP8_SET_QUANT_SMEM(false, kQRows)
-    BFP8_SET_QUANT_SMEM(false, kQCols)
-    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols)
-    BFP8_SET_QUANT_SMEM(true, kQRows)
-    BFP8_SET_QUANT_SMEM(true, kQCols)
-    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols)
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, POW2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    BFP8_SET_QUANT_SMEM(false, kQRows, false)
+    BFP8_SET_QUANT_SMEM(false, kQCols, false)
+    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, false)
+    BFP8_SET_QUANT_SMEM(true, kQRows, false)
+    BFP8_SET_QUANT_SMEM(true, kQCols, false)
+    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, false)
+    BFP8_SET_QUANT_SMEM(false, kQRows, true)
+    BFP8_SET_QUANT_SMEM(false, kQCols, true)
+    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, true)
+    BFP8_SET_QUANT_SMEM(true, kQRows, true)
+    BFP8_SET_QUANT_SMEM(true, kQCols, true)
+    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, true)
 #undef BFP8_SET_QUANT_SMEM
 #define BFP8_SET_GEMM_SMEM(BN, MODE, FUSED)                                                                     \
   if (e == cudaSuccess)                                                                                          \
@@ -326,19 +332,19 @@ bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap&
 // Persistent quantiser grid: two CTAs per SM (each streams its tiles
 // through a 3-deep shared-memory ring).  The tile walk and the TMA
 // coordinates are 32-bit: C up to 2^27 and fewer than 2^31 tiles.
-template <bool kWeight>
+template <bool kWeight, bool kPow2>
 bfp8_status launch_quant_mode(const CUtensorMap& tm, const QuantParams& p, unsigned grid, cudaStream_t st) {
   const int mode = (p.q ? kQRows : 0) | (p.qT ? kQCols : 0);
   if (mode == kQRows)
-    quantize_tile_kernel<kWeight, kQRows><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   else if (mode == kQCols)
-    quantize_tile_kernel<kWeight, kQCols><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQCols, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   else
-    quantize_tile_kernel<kWeight, kQRows | kQCols><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows | kQCols, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   return BFP8_OK;
 }
 
-bfp8_status launch_quant(QuantParams p, bool weight, cudaStream_t st) {
+bfp8_status launch_quant(QuantParams p, bool weight, bool pow2, cudaStream_t st) {
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
@@ -350,7 +356,10 @@ bfp8_status launch_quant(QuantParams p, bool weight, cudaStream_t st) {
   CUtensorMap tm;
   if ((s = make_quant_tmap(&tm, p.x, p.R, p.C)) != BFP8_OK) return s;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
-  s = weight ? launch_quant_mode<true>(tm, p, grid, st) : launch_quant_mode<false>(tm, p, grid, st);
+  if (weight)
+    s = pow2 ? launch_quant_mode<true, true>(tm, p, grid, st) : launch_quant_mode<true, false>(tm, p, grid, st);
+  else
+    s = pow2 ? launch_quant_mode<false, true>(tm, p, grid, st) : launch_quant_mode<false, false>(tm, p, grid, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -413,7 +422,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   if (g.splits == 1) {
     if (Cq == nullptr || fused_here) return BFP8_OK;
     QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns, 0u, 0u};
-    return launch_quant(qp, false, stream);
+    return launch_quant(qp, false, false, stream);
   }
   const int64_t groups = M * (N / 128);
   const int rgrid = static_cast<int>(std::min<int64_t>((groups + 7) / 8, int64_t(dev->sms) * 16));
@@ -423,8 +432,11 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   return cuda_status(cudaGetLastError());
 }
 
+bool scale_mode_ok(int mode) { return mode == BFP8_SCALE_AMAX448 || mode == BFP8_SCALE_POW2; }
+
 bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
-                           cudaStream_t stream) {
+                           int scale_mode, cudaStream_t stream) {
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
   if (!x || (!q && !qT)) return BFP8_EINVAL;
   if ((q && !s) || (qT && !sT)) return BFP8_EINVAL;
   if (!dim_ok(M) || !dim_ok(K)) return BFP8_EINVAL;
@@ -434,10 +446,12 @@ bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, floa
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
   QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns, 0u, 0u};
-  return launch_quant(p, false, stream);
+  return launch_quant(p, false, scale_mode == BFP8_SCALE_POW2, stream);
 }
 
-bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s, cudaStream_t stream) {
+bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s, int scale_mode,
+                         cudaStream_t stream) {
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
   if (!w || !s || (!q && !qT)) return BFP8_EINVAL;
   if (!dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
   if (!aligned16(w) || !aligned16(s) || (q && !aligned16(q)) || (qT && !aligned16(qT))) return BFP8_EALIGN;
@@ -445,7 +459,7 @@ bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
   QuantParams p{static_cast<const uint16_t*>(w), N, K, q, s, qT, nullptr, dev->wait_ns, 0u, 0u};
-  return launch_quant(p, true, stream);
+  return launch_quant(p, true, scale_mode == BFP8_SCALE_POW2, stream);
 }
 
 // Workspace carving for the fused linear calls: consecutive 256-byte aligned
@@ -567,12 +581,22 @@ extern "C" {
 
 bfp8_status bfp8_quantize_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
                                     bfp8_stream_t stream) {
-  return quant_act_impl(x, M, K, q, s, qT, sT, reinterpret_cast<cudaStream_t>(stream));
+  return quant_act_impl(x, M, K, q, s, qT, sT, BFP8_SCALE_AMAX448, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bfp8_status bfp8_quantize_w_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s,
                                     bfp8_stream_t stream) {
-  return quant_w_impl(w, N, K, q, qT, s, reinterpret_cast<cudaStream_t>(stream));
+  return quant_w_impl(w, N, K, q, qT, s, BFP8_SCALE_AMAX448, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_quantize_act_1x128_ex(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT,
+                                       float* sT, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  return quant_act_impl(x, M, K, q, s, qT, sT, scale_mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s,
+                                       bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  return quant_w_impl(w, N, K, q, qT, s, scale_mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B,
@@ -597,9 +621,11 @@ size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return bwd_ws(M, N, K, current_state(), nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
-bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
-                            float* sW, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+bfp8_status bfp8_linear_fwd_ex(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
+                               float* sW, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes,
+                               bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
   if (!X || !W || !Y || !WqT || !sW || !XqT || !sXT) return BFP8_EINVAL;
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
@@ -613,16 +639,22 @@ bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, 
   void* gws;
   fwd_ws(M, N, K, *dev, &cv, &Wq, &Xq, &sX, &gws);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((s = quant_w_impl(W, N, K, Wq, WqT, sW, st)) != BFP8_OK) return s;
-  if ((s = quant_act_impl(X, M, K, Xq, sX, XqT, sXT, st)) != BFP8_OK) return s;
+  if ((s = quant_w_impl(W, N, K, Wq, WqT, sW, scale_mode, st)) != BFP8_OK) return s;
+  if ((s = quant_act_impl(X, M, K, Xq, sX, XqT, sXT, scale_mode, st)) != BFP8_OK) return s;
   const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
   return gemm_impl(BFP8_FPROP, Xq, sX, Wq, sW, M, N, K, Y, nullptr, nullptr, gws, gws_bytes, st);
 }
 
-bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT, const float* sXT,
-                            int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws, size_t ws_bytes,
-                            bfp8_stream_t stream) {
+bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
+                            float* sW, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+  return bfp8_linear_fwd_ex(X, W, M, N, K, Y, WqT, sW, XqT, sXT, ws, ws_bytes, BFP8_SCALE_AMAX448, stream);
+}
+
+bfp8_status bfp8_linear_bwd_ex(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT,
+                               const float* sXT, int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws,
+                               size_t ws_bytes, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
   if (!dY || !WqT || !sW || !XqT || !sXT || !dX || !dW) return BFP8_EINVAL;
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
@@ -637,10 +669,16 @@ bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW,
   bwd_ws(M, N, K, *dev, &cv, &dYq, &sdY, &dYqT, &sdYT, &gws);
   const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((s = quant_act_impl(dY, M, N, dYq, sdY, dYqT, sdYT, st)) != BFP8_OK) return s;
+  if ((s = quant_act_impl(dY, M, N, dYq, sdY, dYqT, sdYT, scale_mode, st)) != BFP8_OK) return s;
   if ((s = gemm_impl(BFP8_DGRAD, dYq, sdY, WqT, sW, M, K, N, dX, nullptr, nullptr, gws, gws_bytes, st)) != BFP8_OK)
     return s;
   return gemm_impl(BFP8_WGRAD, dYqT, sdYT, XqT, sXT, N, K, M, dW, nullptr, nullptr, gws, gws_bytes, st);
+}
+
+bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT, const float* sXT,
+                            int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws, size_t ws_bytes,
+                            bfp8_stream_t stream) {
+  return bfp8_linear_bwd_ex(dY, WqT, sW, XqT, sXT, M, N, K, dX, dW, ws, ws_bytes, BFP8_SCALE_AMAX448, stream);
 }
 
 bfp8_status bfp8_sync_status(bfp8_stream_t stream) {

@@ -219,6 +219,54 @@ __device__ __forceinline__ GroupScale make_group_scale(float amax) {
   return g;
 }
 
+// Power-of-two scale mode: s = 2^k, the smallest power of two with
+// s >= amax/448 (1 for an all-zero group), the reading taken for the paper's
+// SM120 power-of-two scales ("Puro-2B ...", section 3.2).  With
+// amax = (1 + m) 2^e (m the 23-bit fraction, fp32 subnormals normalised),
+// 2^k >= amax/448 = (1 + m)/1.75 * 2^(e-8) holds from k = e - 8 when
+// 1 + m <= 1.75 and from k = e - 7 otherwise.  Then x/s = x * 2^-k is an
+// exact scaling: when 2^-k is a normal fp32 (k >= -127) the product is the
+// IEEE quotient, sign of zero included; smaller scales (only for groups with
+// amax below about 2^-118) take the IEEE division.
+__device__ __forceinline__ GroupScale make_group_scale_pow2(float amax) {
+  GroupScale g;
+  if (!(amax > 0.0f)) {
+    g.s = 1.0f;
+    g.r = 1.0f;
+    g.exact = true;
+    return g;
+  }
+  const uint32_t b = __float_as_uint(amax);
+  int e;
+  uint32_t m;
+  if (b >= 0x00800000u) {
+    e = static_cast<int>(b >> 23) - 127;
+    m = b & 0x007FFFFFu;
+  } else {  // subnormal: amax = b 2^-149
+    const int p = 31 - __clz(static_cast<int>(b));
+    e = p - 149;
+    m = (b << (23 - p)) & 0x007FFFFFu;
+  }
+  const int k = e - 8 + (m > 0x00600000u ? 1 : 0);  // in [-141, 120]
+  g.s = k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23)
+                  : __uint_as_float(1u << (k + 149));
+  g.exact = k >= -127;
+  g.r = g.exact ? __uint_as_float(static_cast<uint32_t>(127 - k) << 23) : 0.0f;
+  return g;
+}
+
+// Whether a group scale of the given mode is on the fast (multiply or FMA)
+// path; restates GroupScale::exact from s alone.
+template <bool kPow2>
+__device__ __forceinline__ bool scale_fast(float s) {
+  return kPow2 ? s >= 0x1p-127f : (s >= 0x1p-80f && s <= 0x1p+100f);
+}
+
+template <bool kPow2>
+__device__ __forceinline__ GroupScale make_scale(float amax) {
+  return kPow2 ? make_group_scale_pow2(amax) : make_group_scale(amax);
+}
+
 // |v| with the sign of x.
 __device__ __forceinline__ float with_sign_of(float v, float x) {
   return __uint_as_float((__float_as_uint(v) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
@@ -255,6 +303,15 @@ __device__ __forceinline__ uint32_t quant4_exact(uint32_t w0, uint32_t w1, float
   const float2 q1 = quotient_pair_unsigned_zero(make_float2(bf16lo(w1), bf16hi(w1)), r2, ns2);
   const uint32_t signs = __byte_perm(w0, w1, 0x7531) & 0x80808080u;
   return e4m3x4(q0.x, q0.y, q1.x, q1.y) | signs;
+}
+
+// Codes of the four bf16 values of words w0, w1 under a power-of-two scale
+// (r2 = 2^-k in both halves): exact products, then the casts.  The product
+// keeps the sign of a zero, so no sign restore is needed.
+__device__ __forceinline__ uint32_t quant4_pow2(uint32_t w0, uint32_t w1, float2 r2) {
+  const float2 a = fmul2(make_float2(bf16lo(w0), bf16hi(w0)), r2);
+  const float2 b = fmul2(make_float2(bf16lo(w1), bf16hi(w1)), r2);
+  return e4m3x4(a.x, a.y, b.x, b.y);
 }
 
 // Codes of the pair (x0, x1) (x0 in the low byte), one group on the FMA path.

@@ -95,11 +95,16 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
 // 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i),
 // one group.  Groups with extreme scales (g.exact false) take the IEEE
 // division.
+template <bool kPow2>
 __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
   if (g.exact) {
     const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-    return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
-                      quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
+    if constexpr (kPow2)
+      return make_uint4(quant4_pow2(w[0], w[1], r2), quant4_pow2(w[2], w[3], r2), quant4_pow2(w[4], w[5], r2),
+                        quant4_pow2(w[6], w[7], r2));
+    else
+      return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
+                        quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
   }
   uint32_t c[8];
 #pragma unroll
@@ -107,18 +112,23 @@ __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupSca
   return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
 }
 
-// The same on the FMA path only (every group of the tile has g.exact).
+// The same on the fast path only (every group of the tile has g.exact).
+template <bool kPow2>
 __device__ __forceinline__ uint4 quant16w_fast(const uint32_t (&w)[8], const GroupScale& g) {
   const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-  return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
-                    quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
+  if constexpr (kPow2)
+    return make_uint4(quant4_pow2(w[0], w[1], r2), quant4_pow2(w[2], w[3], r2), quant4_pow2(w[4], w[5], r2),
+                      quant4_pow2(w[6], w[7], r2));
+  else
+    return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
+                      quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
 }
 
 // 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
-template <bool kFast>
+template <bool kFast, bool kPow2>
 __device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  return kFast ? quant16w_fast(w, g) : quant16w(w, g);
+  return kFast ? quant16w_fast<kPow2>(w, g) : quant16w<kPow2>(w, g);
 }
 
 // Values k and k+1 of one column (element kHalf of word kWord of row slices
@@ -130,17 +140,13 @@ __device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
 }
 
 // 16 codes of one column over 16 rows, one group.  Codes in row order.
-template <int kWord, int kHalf, bool kFast>
+template <int kWord, int kHalf, bool kFast, bool kPow2>
 __device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupScale& g) {
   uint32_t w[8];
 #pragma unroll
   for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
-  return kFast ? quant16w_fast(w, g) : quant16w(w, g);
+  return kFast ? quant16w_fast<kPow2>(w, g) : quant16w<kPow2>(w, g);
 }
-
-// Whether a scale lies in the range where the FMA path is exact (the range
-// make_group_scale tests).
-__device__ __forceinline__ bool scale_on_fma_path(float s) { return s >= 0x1p-80f && s <= 0x1p+100f; }
 
 // Warp 0 fetches tile (rt, ct) into ring slot `buf` with 32 TMA boxes (one
 // per lane; lane 0 arms the slot's barrier first).
@@ -156,29 +162,30 @@ __device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t C, u
 // Codes of this warp's row and column slices of one tile, stored to global
 // memory.  kFast: every group scale of the warp is on the FMA path, so the
 // whole body is one branch-free block the compiler can interleave.
-template <int kMode, bool kFast>
+template <int kMode, bool kFast, bool kPow2>
 __device__ __forceinline__ void quant_tile_codes(const uint4 (&rv)[8], const uint2 (&cv)[16], const GroupScale& grow,
                                                  const GroupScale (&gc)[4], uint8_t* qrow, uint8_t* qcol,
                                                  int64_t R) {
   if constexpr ((kMode & kQRows) != 0) {
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast>(rv[2 * m], rv[2 * m + 1], grow);
+      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast, kPow2>(rv[2 * m], rv[2 * m + 1], grow);
   }
   if constexpr ((kMode & kQCols) != 0) {
     GroupScale g[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_on_fma_path(gc[k].s)};
-    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast>(cv, g[0]);
-    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast>(cv, g[1]);
-    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast>(cv, g[2]);
-    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast>(cv, g[3]);
+    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_fast<kPow2>(gc[k].s)};
+    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast, kPow2>(cv, g[0]);
+    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast, kPow2>(cv, g[1]);
+    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast, kPow2>(cv, g[2]);
+    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast, kPow2>(cv, g[3]);
   }
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
 // kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
-template <bool kWeight, int kMode>
+// kPow2: power-of-two scales (make_group_scale_pow2) instead of amax/448.
+template <bool kWeight, int kMode, bool kPow2>
 __global__ void __launch_bounds__(kQuantThreads, 2)
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       float bm = rbuf[0];
 #pragma unroll
       for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
-      grow = make_group_scale(bm);
+      grow = make_scale<kPow2>(bm);
 #pragma unroll
       for (int k = 0; k < 4; ++k) gc[k] = grow;
       all_exact = grow.exact;  // uniform over the block
@@ -315,7 +322,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     } else {
       bool ok = true;
       if constexpr (kRows) {
-        grow = make_group_scale(row_m);
+        grow = make_scale<kPow2>(row_m);
         ok = grow.exact;
         if (hh == 0) p.s[static_cast<int64_t>(cur.ct) * p.R + r0 + wrow] = grow.s;
       }
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
         // hold those of this lane's columns
         const int sel = g & 3;
         const uint32_t mw = sel < 2 ? m01 : m23;
-        const GroupScale gcol = make_group_scale(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
+        const GroupScale gcol = make_scale<kPow2>(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
         ok = ok && gcol.exact;
         if (g < 4) p.sT[static_cast<int64_t>(cur.rt) * p.C + c0 + 16 * warp + 4 * cq + g] = gcol.s;
 #pragma unroll
@@ -341,9 +348,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     uint8_t* qrow = kRows ? p.q + (r0 + wrow) * p.C + c0 + 16 * hh : nullptr;
     uint8_t* qcol = kCols ? p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg : nullptr;
     if (all_exact)
-      quant_tile_codes<kMode, true>(rv, cv, grow, gc, qrow, qcol, p.R);
+      quant_tile_codes<kMode, true, kPow2>(rv, cv, grow, gc, qrow, qcol, p.R);
     else
-      quant_tile_codes<kMode, false>(rv, cv, grow, gc, qrow, qcol, p.R);
+      quant_tile_codes<kMode, false, kPow2>(rv, cv, grow, gc, qrow, qcol, p.R);
   }
   // Leave no copy in flight into this CTA's shared memory: after an early
   // exit at local tile j, warp 0 (which issues every copy) waits (bounded)

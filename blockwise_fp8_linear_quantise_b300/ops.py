@@ -55,11 +55,23 @@ def _out(t, dtype, shape, device, name):
     return _need(t, dtype, shape, name)
 
 
-def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=None, stream=None):
+SCALE_MODES = {"amax448": 0, "pow2": 1}
+
+
+def _scale_mode(scale_mode):
+    try:
+        return SCALE_MODES[scale_mode]
+    except KeyError:
+        raise ValueError(f"unknown scale_mode {scale_mode!r}") from None
+
+
+def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=None, stream=None,
+                       scale_mode="amax448"):
     """Quantise bf16 x [M, K] in 1x128 groups.
 
     rows   -> q [M, K] uint8 (groups along K), s [K/128, M] float32
     tokens -> qT [K, M] uint8 (groups of 128 tokens per column), sT [M/128, K]
+    scale_mode "amax448" (s = amax/448) or "pow2" (smallest power of two >= amax/448).
     Returns (q, s, qT, sT) with None for outputs not requested.
     """
     M, K = x.shape
@@ -75,20 +87,24 @@ def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=N
     else:
         qT = sT = None
     lib = _lib.load()
-    _check(lib.bfp8_quantize_act_1x128(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _stream(stream)),
+    _check(lib.bfp8_quantize_act_1x128_ex(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT),
+                                          _scale_mode(scale_mode), _stream(stream)),
            "quantize_act_1x128")
     return q, s, qT, sT
 
 
-def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, stream=None):
-    """Quantise bf16 w [N, K] in 128x128 blocks -> (q [N, K], qT [K, N], s [N/128, K/128])."""
+def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, stream=None, scale_mode="amax448"):
+    """Quantise bf16 w [N, K] in 128x128 blocks -> (q [N, K], qT [K, N], s [N/128, K/128]).
+
+    scale_mode as for quantize_act_1x128."""
     N, K = w.shape
     _need(w, torch.bfloat16, (N, K), "w")
     q = _out(q, torch.uint8, (N, K), w.device, "q") if want_q else None
     qT = _out(qT, torch.uint8, (K, N), w.device, "qT") if want_qT else None
     s = _out(s, torch.float32, (N // 128, K // 128), w.device, "s")
     lib = _lib.load()
-    _check(lib.bfp8_quantize_w_128x128(_ptr(w), N, K, _ptr(q), _ptr(qT), _ptr(s), _stream(stream)),
+    _check(lib.bfp8_quantize_w_128x128_ex(_ptr(w), N, K, _ptr(q), _ptr(qT), _ptr(s), _scale_mode(scale_mode),
+                                          _stream(stream)),
            "quantize_w_128x128")
     return q, qT, s
 
@@ -136,9 +152,10 @@ def linear_bwd_workspace_bytes(M, N, K):
     return int(_lib.load().bfp8_linear_bwd_workspace_bytes(M, N, K))
 
 
-def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None):
+def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None, scale_mode="amax448"):
     """Y = X . W^T through the fused forward.  Returns (Y, saved) where saved
-    holds WqT, sW, XqT, sXT for linear_bwd."""
+    holds WqT, sW, XqT, sXT for linear_bwd.  scale_mode as for
+    quantize_act_1x128."""
     M, K = X.shape
     N = W.shape[0]
     _need(X, torch.bfloat16, (M, K), "X")
@@ -153,14 +170,15 @@ def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(linear_fwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     lib = _lib.load()
-    _check(lib.bfp8_linear_fwd(_ptr(X), _ptr(W), M, N, K, _ptr(Y), _ptr(saved["WqT"]), _ptr(saved["sW"]),
-                               _ptr(saved["XqT"]), _ptr(saved["sXT"]), _ptr(workspace), workspace.numel(),
-                               _stream(stream)), "linear_fwd")
+    _check(lib.bfp8_linear_fwd_ex(_ptr(X), _ptr(W), M, N, K, _ptr(Y), _ptr(saved["WqT"]), _ptr(saved["sW"]),
+                                  _ptr(saved["XqT"]), _ptr(saved["sXT"]), _ptr(workspace), workspace.numel(),
+                                  _scale_mode(scale_mode), _stream(stream)), "linear_fwd")
     return Y, saved
 
 
-def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None):
-    """(dX, dW) for the layer whose forward produced ``saved``."""
+def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None, scale_mode="amax448"):
+    """(dX, dW) for the layer whose forward produced ``saved``; scale_mode
+    applies to the quantisation of dY."""
     M, N = dY.shape
     K = saved["WqT"].shape[0]
     _need(dY, torch.bfloat16, (M, N), "dY")
@@ -174,9 +192,9 @@ def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None):
     if workspace is None:
         workspace = torch.empty(linear_bwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     lib = _lib.load()
-    _check(lib.bfp8_linear_bwd(_ptr(dY), _ptr(saved["WqT"]), _ptr(saved["sW"]), _ptr(saved["XqT"]),
-                               _ptr(saved["sXT"]), M, N, K, _ptr(dX), _ptr(dW), _ptr(workspace), workspace.numel(),
-                               _stream(stream)), "linear_bwd")
+    _check(lib.bfp8_linear_bwd_ex(_ptr(dY), _ptr(saved["WqT"]), _ptr(saved["sW"]), _ptr(saved["XqT"]),
+                                  _ptr(saved["sXT"]), M, N, K, _ptr(dX), _ptr(dW), _ptr(workspace),
+                                  workspace.numel(), _scale_mode(scale_mode), _stream(stream)), "linear_bwd")
     return dX, dW
 
 

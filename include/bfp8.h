@@ -63,6 +63,12 @@ typedef enum {
   BFP8_WGRAD = 2  /* dW = dY^T . X : reduction over tokens       */
 } bfp8_layout;
 
+/* How a group's scale s is chosen from its amax (the largest |x|). */
+typedef enum {
+  BFP8_SCALE_AMAX448 = 0, /* s = fp32(amax / 448): the default, used by every entry point without _ex */
+  BFP8_SCALE_POW2 = 1     /* s = smallest power of two >= amax / 448 (the paper's SM120 power-of-two scales) */
+} bfp8_scale_mode;
+
 /*
  * Activation / activation-gradient quantiser, 1x128 groups (section 3.2:
  * groups of 128 consecutive values along the GEMM reduction dimension).
@@ -97,6 +103,27 @@ bfp8_status bfp8_quantize_act_1x128(const void* x, int64_t M, int64_t K,
 bfp8_status bfp8_quantize_w_128x128(const void* w, int64_t N, int64_t K,
                                     uint8_t* q, uint8_t* qT, float* s,
                                     bfp8_stream_t stream);
+
+/*
+ * The two quantisers above with an explicit scale rule ("Puro-2B ...",
+ * section 3.2: the same 1x128 / 128x128 grouping runs on SM120 with
+ * power-of-two scales).  Arguments, layouts, ownership and errors are those of
+ * bfp8_quantize_act_1x128 and bfp8_quantize_w_128x128; scale_mode selects s:
+ *   BFP8_SCALE_AMAX448  s = fp32(amax / 448) (identical to the calls above);
+ *   BFP8_SCALE_POW2     s = 2^k, the smallest power of two with s >= amax/448
+ *                       (so nothing saturates and the group's largest |x|/s
+ *                       lies in (224, 448]); 1 for an all-zero group.
+ * In both modes q = E4M3_rn_satfinite(fp32(x / s)); with a power-of-two s the
+ * division is an exact scaling.  The scales are fp32 in both modes, so the
+ * GEMM and linear entry points consume either.  An unknown scale_mode returns
+ * BFP8_EINVAL.
+ */
+bfp8_status bfp8_quantize_act_1x128_ex(const void* x, int64_t M, int64_t K,
+                                       uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                       bfp8_scale_mode scale_mode, bfp8_stream_t stream);
+bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K,
+                                       uint8_t* q, uint8_t* qT, float* s,
+                                       bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
  * Block-scaled FP8 GEMM with fp32 promotion per 128-deep slice (section 3.2:
@@ -201,6 +228,28 @@ bfp8_status bfp8_linear_bwd(const void* dY,
                             void* ws, size_t ws_bytes,
                             bfp8_stream_t stream);
 size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * bfp8_linear_fwd / bfp8_linear_bwd with an explicit scale rule for every
+ * quantisation they run (see bfp8_quantize_act_1x128_ex).  The saved tensors
+ * carry fp32 scales in either mode; bfp8_linear_bwd_ex takes the mode for
+ * the output-gradient quantisation only.  Arguments, workspaces and errors
+ * are otherwise those of the calls without _ex; an unknown scale_mode
+ * returns BFP8_EINVAL.
+ */
+bfp8_status bfp8_linear_fwd_ex(const void* X, const void* W,
+                               int64_t M, int64_t N, int64_t K,
+                               void* Y,
+                               uint8_t* WqT, float* sW, uint8_t* XqT, float* sXT,
+                               void* ws, size_t ws_bytes,
+                               bfp8_scale_mode scale_mode, bfp8_stream_t stream);
+bfp8_status bfp8_linear_bwd_ex(const void* dY,
+                               const uint8_t* WqT, const float* sW,
+                               const uint8_t* XqT, const float* sXT,
+                               int64_t M, int64_t N, int64_t K,
+                               void* dX, void* dW,
+                               void* ws, size_t ws_bytes,
+                               bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

@@ -1,4 +1,5 @@
-"""GPU quantisers vs the CPU oracle: E4M3 codes and fp32 scales bit-exact."""
+"""GPU quantisers vs the CPU oracle: E4M3 codes and fp32 scales bit-exact, in
+both scale modes (amax/448 and the power-of-two mode)."""
 
 import numpy as np
 import pytest
@@ -11,34 +12,34 @@ from blockwise_fp8_linear_quantise_b300 import ops, workloads
 pytestmark = pytest.mark.gpu
 
 
-def check_act(x_bf16):
+def check_act(x_bf16, scale_mode="amax448"):
     x = x_bf16.to(dev())
-    q, s, qT, sT = ops.quantize_act_1x128(x, rows=True, tokens=True)
+    q, s, qT, sT = ops.quantize_act_1x128(x, rows=True, tokens=True, scale_mode=scale_mode)
     torch.cuda.synchronize()
     assert ops.sync_status() == 0
     xn = np32(x_bf16)
-    oq, os_ = quant.quantize_act_1x128(xn)
-    oqT, osT = quant.quantize_act_tokens_1x128(xn)
+    oq, os_ = quant.quantize_act_1x128(xn, scale_mode=scale_mode)
+    oqT, osT = quant.quantize_act_tokens_1x128(xn, scale_mode=scale_mode)
     assert_codes_equal(u8(q), oq, "q")
     assert_scales_equal(s.cpu().numpy(), os_, "s")
     assert_codes_equal(u8(qT), oqT, "qT")
     assert_scales_equal(sT.cpu().numpy(), osT, "sT")
     # single-output variants give the same bytes
-    q2, s2, _, _ = ops.quantize_act_1x128(x, rows=True, tokens=False)
-    _, _, qT2, sT2 = ops.quantize_act_1x128(x, rows=False, tokens=True)
+    q2, s2, _, _ = ops.quantize_act_1x128(x, rows=True, tokens=False, scale_mode=scale_mode)
+    _, _, qT2, sT2 = ops.quantize_act_1x128(x, rows=False, tokens=True, scale_mode=scale_mode)
     assert torch.equal(q2, q) and torch.equal(s2, s) and torch.equal(qT2, qT) and torch.equal(sT2, sT)
 
 
-def check_w(w_bf16):
+def check_w(w_bf16, scale_mode="amax448"):
     w = w_bf16.to(dev())
-    q, qT, s = ops.quantize_w_128x128(w)
+    q, qT, s = ops.quantize_w_128x128(w, scale_mode=scale_mode)
     assert ops.sync_status() == 0
-    oq, oqT, os_ = quant.quantize_w_128x128(np32(w_bf16))
+    oq, oqT, os_ = quant.quantize_w_128x128(np32(w_bf16), scale_mode=scale_mode)
     assert_codes_equal(u8(q), oq, "Wq")
     assert_codes_equal(u8(qT), oqT, "WqT")
     assert_scales_equal(s.cpu().numpy(), os_, "sW")
-    q1, _, s1 = ops.quantize_w_128x128(w, want_qT=False)
-    _, qT1, _ = ops.quantize_w_128x128(w, want_q=False)
+    q1, _, s1 = ops.quantize_w_128x128(w, want_qT=False, scale_mode=scale_mode)
+    _, qT1, _ = ops.quantize_w_128x128(w, want_q=False, scale_mode=scale_mode)
     assert torch.equal(q1, q) and torch.equal(qT1, qT) and torch.equal(s1, s)
 
 
@@ -55,7 +56,8 @@ def test_multi_tile_shapes(M, K):
     check_w(x)
 
 
-def test_edge_values():
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+def test_edge_values(scale_mode):
     # zeros (scale 1), signed zeros, subnormal-scale groups, huge groups, ties
     M, K = 256, 384
     x = np.zeros((M, K), np.float32)
@@ -72,18 +74,19 @@ def test_edge_values():
     fin = bits[np.isfinite(bits)]
     x[128:256, 256:384].flat[: min(fin.size, 128 * 128)] = fin[: 128 * 128]
     xb = workloads.to_bf16(x)
-    check_act(xb)
-    check_w(xb)
+    check_act(xb, scale_mode)
+    check_w(xb, scale_mode)
 
 
-def test_every_bf16_bit_pattern():
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+def test_every_bf16_bit_pattern(scale_mode):
     bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
     fin = bits[np.isfinite(bits)]
     x = np.zeros((512, 256), np.float32)
     x.flat[: fin.size] = fin
     xb = workloads.to_bf16(x)
-    check_act(xb)
-    check_w(xb)
+    check_act(xb, scale_mode)
+    check_w(xb, scale_mode)
 
 
 @pytest.mark.parametrize("amax", [3.0, 0.7109375, 123.5, 1.0e-30, 5.0e-39, 2.5e38, 3.5, 1.0])
@@ -111,7 +114,8 @@ def test_every_bf16_value_below_a_fixed_amax(amax):
     check_w(xb)
 
 
-def test_every_bf16_value_as_group_amax():
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+def test_every_bf16_value_as_group_amax(scale_mode):
     """Row group g (128 values along K) has amax = the g-th positive finite
     bf16 value, so every scale amax/448 reachable from bf16 inputs is formed
     once (normal and subnormal quotients alike); the other 127 values of the
@@ -129,7 +133,7 @@ def test_every_bf16_value_as_group_amax():
     full = np.zeros((n, 128), np.float32)
     full[: amax.size] = xb.float().numpy()
     x = workloads.to_bf16(full.reshape(-1, 256))
-    check_act(x)
+    check_act(x, scale_mode)
 
 
 @pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_gateup", "w"), ("mlp_down", "x"),
@@ -148,3 +152,65 @@ def test_stack_layer_tensors():
     check_act(workloads.tensor(wl, "x_f"))
     check_act(workloads.tensor(wl, "dy_gu"))
     check_w(workloads.tensor(wl, "w_gu", layer=27))
+
+
+# ---------------------------------------------------------------- power of two
+
+
+@pytest.mark.parametrize("amax", [3.0, 3.5, 0.7109375, 1.0e-30, 5.0e-39, 2.5e38, 448.0, 449.0])
+def test_pow2_every_bf16_value_below_a_fixed_amax(amax):
+    """As the amax/448 sweep, with power-of-two scales: x / s is exact, and
+    amax 5e-39 gives a scale below 2^-127, which takes the division path."""
+    a = np.float32(workloads.to_bf16(np.array([amax], np.float32)).float().numpy()[0])
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = bits[np.isfinite(bits) & (np.abs(bits) <= a)]
+    per = 127
+    groups = -(-vals.size // per)
+    groups += (-groups) % 2
+    padded = np.zeros(groups * per, np.float32)
+    padded[: vals.size] = vals
+    g = padded.reshape(groups, per)
+    first = np.where(np.arange(groups) % 2 == 0, a, -a).astype(np.float32)[:, None]
+    x = np.concatenate([first, g], axis=1).reshape(-1, 256)
+    rows = -(-x.shape[0] // 128) * 128
+    full = np.zeros((rows, 256), np.float32)
+    full[: x.shape[0]] = x
+    xb = workloads.to_bf16(full)
+    check_act(xb, "pow2")
+    check_w(xb, "pow2")
+
+
+@pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_down", "dy"), ("attn_proj", "w_qkv")])
+def test_pow2_full_size_configs(name, tag):
+    t = bf16_input(name, tag)
+    if tag.startswith("w"):
+        check_w(t, "pow2")
+    else:
+        check_act(t, "pow2")
+
+
+def test_pow2_linear_layer_against_oracle():
+    """Power-of-two scales flow through the unchanged GEMM: FPROP of a
+    pow2-quantised layer matches the oracle's GEMM on the oracle's own pow2
+    quantisation within the GEMM tolerance."""
+    from gpu_helpers import REL_FRO_TOL, rel_fro
+    from oracle import gemm as ogemm
+    x, w = bf16_input("tiny", "x"), bf16_input("tiny", "w")
+    Xq, sX, _, _ = ops.quantize_act_1x128(x.to(dev()), rows=True, tokens=False, scale_mode="pow2")
+    Wq, _, sW = ops.quantize_w_128x128(w.to(dev()), want_qT=False, scale_mode="pow2")
+    Y = ops.fp8_block_gemm(ops.FPROP, Xq, sX, Wq, sW)
+    assert ops.sync_status() == 0
+    oq, os_ = quant.quantize_act_1x128(np32(x), scale_mode="pow2")
+    wq, _, ws = quant.quantize_w_128x128(np32(w), scale_mode="pow2")
+    want = ogemm.fprop(oq, os_, wq, ws)[1]
+    assert rel_fro(np32(Y), want) <= REL_FRO_TOL
+
+
+def test_unknown_scale_mode_is_rejected():
+    from blockwise_fp8_linear_quantise_b300 import _lib
+    x = torch.zeros((128, 128), dtype=torch.bfloat16, device=dev())
+    q = torch.empty((128, 128), dtype=torch.uint8, device=dev())
+    s = torch.empty((1, 128), dtype=torch.float32, device=dev())
+    st = torch.cuda.current_stream().cuda_stream
+    assert _lib.load().bfp8_quantize_act_1x128_ex(x.data_ptr(), 128, 128, q.data_ptr(), s.data_ptr(), None, None,
+                                                  7, st) == 1
