@@ -112,6 +112,18 @@ def wgrad(dYqT, sdYT, XqT, sXT, rows=None, cols=None):
         rows, cols)
 
 
+def accumulate_into(main, acc):
+    """fp32 accumulate-into: main_new = f32(main + acc), one IEEE addition per
+    element.
+
+    acc is the GEMM's fp32 promotion accumulator (before the bf16 rounding of
+    the plain output).  This is how a weight gradient lands in an fp32 main
+    gradient: section 3.2 keeps the training state on the BF16/FP32 path and
+    uses FP8 only as the online compute format of the linear layers.
+    """
+    return (np.asarray(main, dtype=np.float32) + np.asarray(acc, dtype=np.float32)).astype(np.float32)
+
+
 def linear_fwd(X, W):
     """Quantise W (128x128) and X (1x128 along features, and along tokens for
     the later wgrad), then run fprop.
@@ -128,11 +140,15 @@ def linear_fwd(X, W):
     return Y, saved
 
 
-def linear_bwd(dY, saved):
+def linear_bwd(dY, saved, main_grad=None):
     """Quantise dY along features (for dgrad) and along tokens (for wgrad),
-    then run dgrad and wgrad.  Returns (dX, dW) as bf16-valued float32."""
+    then run dgrad and wgrad.  Returns (dX, dW) as bf16-valued float32; with
+    main_grad (fp32 [N, K]) dW is instead main_grad + the wgrad accumulator
+    (accumulate_into), returned as a new float32 array."""
     dYq, sdY = quant.quantize_act_1x128(dY)
     dYqT, sdYT = quant.quantize_act_tokens_1x128(dY)
     _, dX = dgrad(dYq, sdY, saved["WqT"], saved["sW"])
-    _, dW = wgrad(dYqT, sdYT, saved["XqT"], saved["sXT"])
+    acc, dW = wgrad(dYqT, sdYT, saved["XqT"], saved["sXT"])
+    if main_grad is not None:
+        dW = accumulate_into(main_grad, acc)
     return dX, dW

@@ -153,3 +153,41 @@ def test_quantised_product_close_to_unquantised():
     ref = X.astype(np.float64) @ W.astype(np.float64).T
     rel = np.linalg.norm(Y - ref) / np.linalg.norm(ref)
     assert 1e-3 < rel < 0.08
+
+
+# ------------------------------------------------------- fp32 accumulate-into
+
+
+def test_accumulate_into_hand_worked_sums():
+    """One IEEE fp32 addition per element, checked on sums worked by hand:
+    exact ones, a tie that rounds to even and one that rounds up."""
+    main = np.array([1.0, -2.5, 1.0, 1.0, 3.0e38, 0.0], np.float32)
+    acc = np.array([2.0, 0.75, 2.0 ** -24, 3 * 2.0 ** -24, 3.0e38, -0.0], np.float32)
+    want = np.array([3.0, -1.75, 1.0, 1.0 + 2.0 ** -22, np.inf, 0.0], np.float32)
+    # 1 + 2^-24: exactly halfway between 1 and 1 + 2^-23, ties to even -> 1
+    # 1 + 3*2^-24: halfway between 1 + 2^-23 and 1 + 2^-22, ties to even -> 1 + 2^-22
+    with np.errstate(over="ignore"):
+        got = gemm.accumulate_into(main, acc)
+    assert np.array_equal(got, want) and got.dtype == np.float32
+    assert np.signbit(got[5]) == False  # +0 + -0 = +0
+
+
+def test_linear_bwd_main_grad_adds_the_wgrad_accumulator():
+    wl = workloads.make("tiny")
+    x = workloads.tensor(wl, "x").float().numpy()
+    w = workloads.tensor(wl, "w").float().numpy()
+    dy = (np.random.default_rng(3).standard_normal((256, 256)) * 1e-3).astype(np.float32)
+    dy = torch.from_numpy(dy).to(torch.bfloat16).float().numpy()
+    _, saved = gemm.linear_fwd(x, w)
+    dX, dW = gemm.linear_bwd(dy, saved)
+    main0 = np.random.default_rng(4).standard_normal((256, 256)).astype(np.float32)
+    dX2, main1 = gemm.linear_bwd(dy, saved, main_grad=main0)
+    assert np.array_equal(dX, dX2)
+    # the increment is the fp32 accumulator, whose bf16 rounding is dW
+    dYqT, sdYT = quant.quantize_act_tokens_1x128(dy)
+    acc, _ = gemm.wgrad(dYqT, sdYT, saved["XqT"], saved["sXT"])
+    assert np.array_equal(main1, (main0.astype(np.float64) + acc).astype(np.float32))
+    assert np.array_equal(torch.from_numpy(acc).to(torch.bfloat16).float().numpy(), dW)
+    # zero main gradient: accumulate-into returns the accumulator itself
+    _, main_z = gemm.linear_bwd(dy, saved, main_grad=np.zeros_like(main0))
+    assert np.array_equal(main_z, acc)
