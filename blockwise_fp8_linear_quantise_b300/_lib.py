@@ -19,6 +19,7 @@ SIGNATURES = {
     "bfp8_quantize_w_128x128_ex": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_int, c_p]),
     "bfp8_fp8_block_gemm": (c_int, [c_int, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "bfp8_gemm_workspace_bytes": (c_sz, [c_int, c_i64, c_i64, c_i64]),
+    "bfp8_fp8_block_gemm_accumulate": (c_int, [c_int, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_sz, c_p]),
     "bfp8_fp8_block_gemm_noalloc": (c_int, [c_int, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p]),
     "bfp8_linear_fwd": (c_int, [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "bfp8_linear_fwd_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64]),
@@ -26,6 +27,8 @@ SIGNATURES = {
     "bfp8_linear_bwd_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "bfp8_linear_fwd_ex": (c_int, [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_int, c_p]),
     "bfp8_linear_bwd_ex": (c_int, [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_sz, c_int, c_p]),
+    "bfp8_linear_bwd_main_grad": (c_int, [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_sz, c_int,
+                                          c_p]),
     "bfp8_sync_status": (c_int, [c_p]),
     "bfp8_set_wait_limit_ns": (c_int, [ctypes.c_uint64]),
     "bfp8_set_gemm_kernel": (c_int, [c_int]),

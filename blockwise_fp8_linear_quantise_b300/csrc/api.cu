@@ -87,65 +87,83 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_SET_QUANT_SMEM(true, kQCols, true)
     BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, true)
 #undef BFP8_SET_QUANT_SMEM
-#define BFP8_SET_GEMM_SMEM(BN, MODE, FUSED)                                                                     \
-  if (e == cudaSuccess)                                                                                          \
-    e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define BFP8_SET_GEMM_SMEM(BN, MODE, EPI)                                                                     \
+  if (e == cudaSuccess)                                                                                        \
+    e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              GemmSmem<BN>::kAlloc);
-    BFP8_SET_GEMM_SMEM(256, kSbBlock, false)
-    BFP8_SET_GEMM_SMEM(256, kSbBlockT, false)
-    BFP8_SET_GEMM_SMEM(256, kSbCol, false)
-    BFP8_SET_GEMM_SMEM(256, kSbBlock, true)
-    BFP8_SET_GEMM_SMEM(256, kSbBlockT, true)
-    BFP8_SET_GEMM_SMEM(256, kSbCol, true)
-    BFP8_SET_GEMM_SMEM(128, kSbBlock, false)
-    BFP8_SET_GEMM_SMEM(128, kSbBlockT, false)
-    BFP8_SET_GEMM_SMEM(128, kSbCol, false)
+    BFP8_SET_GEMM_SMEM(256, kSbBlock, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(256, kSbCol, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(256, kSbBlock, kEpiCodes)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT, kEpiCodes)
+    BFP8_SET_GEMM_SMEM(256, kSbCol, kEpiCodes)
+    BFP8_SET_GEMM_SMEM(256, kSbBlock, kEpiAccum)
+    BFP8_SET_GEMM_SMEM(256, kSbBlockT, kEpiAccum)
+    BFP8_SET_GEMM_SMEM(256, kSbCol, kEpiAccum)
+    BFP8_SET_GEMM_SMEM(128, kSbBlock, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(128, kSbBlockT, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(128, kSbCol, kEpiPlain)
+    BFP8_SET_GEMM_SMEM(128, kSbBlock, kEpiAccum)
+    BFP8_SET_GEMM_SMEM(128, kSbBlockT, kEpiAccum)
+    BFP8_SET_GEMM_SMEM(128, kSbCol, kEpiAccum)
 #undef BFP8_SET_GEMM_SMEM
-#define BFP8_SET_PAIR_SMEM(MODE, FUSED)                                                                        \
-  if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+#define BFP8_SET_PAIR_SMEM(MODE, EPI)                                                                        \
+  if (e == cudaSuccess)                                                                                       \
+    e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              GemmSmem<256, true>::kAlloc);
-    BFP8_SET_PAIR_SMEM(kSbBlock, false)
-    BFP8_SET_PAIR_SMEM(kSbBlockT, false)
-    BFP8_SET_PAIR_SMEM(kSbCol, false)
-    BFP8_SET_PAIR_SMEM(kSbBlock, true)
-    BFP8_SET_PAIR_SMEM(kSbBlockT, true)
-    BFP8_SET_PAIR_SMEM(kSbCol, true)
+    BFP8_SET_PAIR_SMEM(kSbBlock, kEpiPlain)
+    BFP8_SET_PAIR_SMEM(kSbBlockT, kEpiPlain)
+    BFP8_SET_PAIR_SMEM(kSbCol, kEpiPlain)
+    BFP8_SET_PAIR_SMEM(kSbBlock, kEpiCodes)
+    BFP8_SET_PAIR_SMEM(kSbBlockT, kEpiCodes)
+    BFP8_SET_PAIR_SMEM(kSbCol, kEpiCodes)
+    BFP8_SET_PAIR_SMEM(kSbBlock, kEpiAccum)
+    BFP8_SET_PAIR_SMEM(kSbBlockT, kEpiAccum)
+    BFP8_SET_PAIR_SMEM(kSbCol, kEpiAccum)
 #undef BFP8_SET_PAIR_SMEM
     if (e != cudaSuccess) return BFP8_ECUDA;
     // The GEMM moves registers between warpgroups with setmaxnreg; that is
     // only safe if each thread really starts with kLaunchRegs registers.
     // Refuse to run a build where it does not (it would wait forever).
-#define BFP8_CHECK_REGS(BN, MODE, FUSED)                                                  \
+#define BFP8_CHECK_REGS(BN, MODE, EPI)                                                  \
+  {                                                                                      \
+    cudaFuncAttributes fa;                                                               \
+    if (cudaFuncGetAttributes(&fa, block_gemm_kernel<BN, MODE, EPI>) != cudaSuccess) \
+      return BFP8_ECUDA;                                                                 \
+    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                             \
+  }
+    BFP8_CHECK_REGS(256, kSbBlock, kEpiPlain)
+    BFP8_CHECK_REGS(256, kSbBlockT, kEpiPlain)
+    BFP8_CHECK_REGS(256, kSbCol, kEpiPlain)
+    BFP8_CHECK_REGS(256, kSbBlock, kEpiCodes)
+    BFP8_CHECK_REGS(256, kSbBlockT, kEpiCodes)
+    BFP8_CHECK_REGS(256, kSbCol, kEpiCodes)
+    BFP8_CHECK_REGS(256, kSbBlock, kEpiAccum)
+    BFP8_CHECK_REGS(256, kSbBlockT, kEpiAccum)
+    BFP8_CHECK_REGS(256, kSbCol, kEpiAccum)
+    BFP8_CHECK_REGS(128, kSbBlock, kEpiPlain)
+    BFP8_CHECK_REGS(128, kSbBlockT, kEpiPlain)
+    BFP8_CHECK_REGS(128, kSbCol, kEpiPlain)
+    BFP8_CHECK_REGS(128, kSbBlock, kEpiAccum)
+    BFP8_CHECK_REGS(128, kSbBlockT, kEpiAccum)
+    BFP8_CHECK_REGS(128, kSbCol, kEpiAccum)
+#undef BFP8_CHECK_REGS
+#define BFP8_CHECK_PAIR_REGS(MODE, EPI)                                                   \
   {                                                                                        \
     cudaFuncAttributes fa;                                                                 \
-    if (cudaFuncGetAttributes(&fa, block_gemm_kernel<BN, MODE, FUSED>) != cudaSuccess) \
+    if (cudaFuncGetAttributes(&fa, block_gemm_pair_kernel<MODE, EPI>) != cudaSuccess) \
       return BFP8_ECUDA;                                                                   \
     if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                               \
   }
-    BFP8_CHECK_REGS(256, kSbBlock, false)
-    BFP8_CHECK_REGS(256, kSbBlockT, false)
-    BFP8_CHECK_REGS(256, kSbCol, false)
-    BFP8_CHECK_REGS(256, kSbBlock, true)
-    BFP8_CHECK_REGS(256, kSbBlockT, true)
-    BFP8_CHECK_REGS(256, kSbCol, true)
-    BFP8_CHECK_REGS(128, kSbBlock, false)
-    BFP8_CHECK_REGS(128, kSbBlockT, false)
-    BFP8_CHECK_REGS(128, kSbCol, false)
-#undef BFP8_CHECK_REGS
-#define BFP8_CHECK_PAIR_REGS(MODE, FUSED)                                                   \
-  {                                                                                          \
-    cudaFuncAttributes fa;                                                                   \
-    if (cudaFuncGetAttributes(&fa, block_gemm_pair_kernel<MODE, FUSED>) != cudaSuccess) \
-      return BFP8_ECUDA;                                                                     \
-    if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;                                 \
-  }
-    BFP8_CHECK_PAIR_REGS(kSbBlock, false)
-    BFP8_CHECK_PAIR_REGS(kSbBlockT, false)
-    BFP8_CHECK_PAIR_REGS(kSbCol, false)
-    BFP8_CHECK_PAIR_REGS(kSbBlock, true)
-    BFP8_CHECK_PAIR_REGS(kSbBlockT, true)
-    BFP8_CHECK_PAIR_REGS(kSbCol, true)
+    BFP8_CHECK_PAIR_REGS(kSbBlock, kEpiPlain)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT, kEpiPlain)
+    BFP8_CHECK_PAIR_REGS(kSbCol, kEpiPlain)
+    BFP8_CHECK_PAIR_REGS(kSbBlock, kEpiCodes)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT, kEpiCodes)
+    BFP8_CHECK_PAIR_REGS(kSbCol, kEpiCodes)
+    BFP8_CHECK_PAIR_REGS(kSbBlock, kEpiAccum)
+    BFP8_CHECK_PAIR_REGS(kSbBlockT, kEpiAccum)
+    BFP8_CHECK_PAIR_REGS(kSbCol, kEpiAccum)
 #undef BFP8_CHECK_PAIR_REGS
     // How many CTA pairs can be resident at once (the persistent pair grid).
     {
@@ -203,6 +221,19 @@ bfp8_status make_quant_tmap(CUtensorMap* map, const void* x, int64_t R, int64_t 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
+}
+
+// fp32 [rows, cols] accumulation target, box 32 columns x 32 rows, 128-byte
+// swizzle (the accumulate epilogue's staging layout).
+bfp8_status make_f32_acc_tmap(CUtensorMap* map, float* base, int64_t rows, int64_t cols) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
 }
@@ -267,64 +298,76 @@ GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const De
   return g;
 }
 
-template <int BN, bool kFused>
+template <int BN, int kEpi>
 void launch_gemm_bn_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const GemmParams& p, int grid, cudaStream_t st) {
   const int smem = GemmSmem<BN>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_kernel<BN, kSbBlock, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlock, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_kernel<BN, kSbBlockT, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlockT, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_kernel<BN, kSbCol, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbCol, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
   }
 }
 
-// p.Cq set (one split, BN = 256 only) selects the instance with the fused
-// E4M3 epilogue.
+// The epilogue kind of a launch: fp32 accumulate with p.Cacc and one split,
+// the E4M3 codes with p.Cq (one split, BN = 256 only), bf16 C (or split-K
+// partials) otherwise.
+int epi_kind(const GemmParams& p) {
+  if (p.Cacc != nullptr && p.splits == 1) return kEpiAccum;
+  if (p.Cq != nullptr) return kEpiCodes;
+  return kEpiPlain;
+}
+
 template <int BN>
 bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                            const GemmParams& p, int grid, cudaStream_t st) {
-  if constexpr (BN == 256) {
-    if (p.Cq != nullptr)
-      launch_gemm_bn_mode<BN, true>(mode, ta, tb, tc, p, grid, st);
+  const int epi = epi_kind(p);
+  if (epi == kEpiAccum) {
+    launch_gemm_bn_mode<BN, kEpiAccum>(mode, ta, tb, tc, p, grid, st);
+  } else if (epi == kEpiCodes) {
+    if constexpr (BN == 256)
+      launch_gemm_bn_mode<BN, kEpiCodes>(mode, ta, tb, tc, p, grid, st);
     else
-      launch_gemm_bn_mode<BN, false>(mode, ta, tb, tc, p, grid, st);
+      return BFP8_EINVAL;
   } else {
-    if (p.Cq != nullptr) return BFP8_EINVAL;
-    launch_gemm_bn_mode<BN, false>(mode, ta, tb, tc, p, grid, st);
+    launch_gemm_bn_mode<BN, kEpiPlain>(mode, ta, tb, tc, p, grid, st);
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
 
-template <bool kFused>
+template <int kEpi>
 void launch_gemm_pair_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                            const GemmParams& p, int grid, cudaStream_t st) {
   const int smem = GemmSmem<256, true>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_pair_kernel<kSbBlock, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlock, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_pair_kernel<kSbBlockT, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlockT, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_pair_kernel<kSbCol, kFused><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbCol, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
       break;
   }
 }
 
 bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                              const GemmParams& p, int grid, cudaStream_t st) {
-  if (p.Cq != nullptr)
-    launch_gemm_pair_mode<true>(mode, ta, tb, tc, p, grid, st);
+  const int epi = epi_kind(p);
+  if (epi == kEpiAccum)
+    launch_gemm_pair_mode<kEpiAccum>(mode, ta, tb, tc, p, grid, st);
+  else if (epi == kEpiCodes)
+    launch_gemm_pair_mode<kEpiCodes>(mode, ta, tb, tc, p, grid, st);
   else
-    launch_gemm_pair_mode<false>(mode, ta, tb, tc, p, grid, st);
+    launch_gemm_pair_mode<kEpiPlain>(mode, ta, tb, tc, p, grid, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -364,15 +407,17 @@ bfp8_status launch_quant(QuantParams p, bool weight, bool pow2, cudaStream_t st)
   return cuda_status(cudaGetLastError());
 }
 
+// C (bf16) is written, or (with Cacc, C null) the result is added into the
+// fp32 Cacc; exactly one of the two.
 bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
                       int64_t M, int64_t N, int64_t K, void* C, uint8_t* Cq, float* sCq, void* ws, size_t ws_bytes,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, float* Cacc = nullptr) {
   if (layout != BFP8_FPROP && layout != BFP8_DGRAD && layout != BFP8_WGRAD) return BFP8_EINVAL;
-  if (!A || !sa || !B || !sb || !C) return BFP8_EINVAL;
-  if ((Cq == nullptr) != (sCq == nullptr)) return BFP8_EINVAL;
+  if (!A || !sa || !B || !sb || ((C == nullptr) == (Cacc == nullptr))) return BFP8_EINVAL;
+  if ((Cq == nullptr) != (sCq == nullptr) || (Cacc && Cq)) return BFP8_EINVAL;
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(sa) || !aligned16(sb) || !aligned16(C) ||
-      (Cq && (!aligned16(Cq) || !aligned16(sCq))))
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sa) || !aligned16(sb) || (C && !aligned16(C)) ||
+      (Cacc && !aligned16(Cacc)) || (Cq && (!aligned16(Cq) || !aligned16(sCq))))
     return BFP8_EALIGN;
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
@@ -385,7 +430,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   CUtensorMap ta, tb, tc;
   if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
   if ((s = make_kmajor_tmap(&tb, B, N, K, g.pair ? g.bn / 2 : g.bn)) != BFP8_OK) return s;
-  if ((s = make_bf16_store_tmap(&tc, C, M, N)) != BFP8_OK) return s;
+  if ((s = Cacc ? make_f32_acc_tmap(&tc, Cacc, M, N) : make_bf16_store_tmap(&tc, C, M, N)) != BFP8_OK) return s;
 
   GemmParams p;
   p.M = static_cast<int>(M);
@@ -402,6 +447,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   p.sa = sa;
   p.sb = sb;
   p.C = static_cast<uint16_t*>(C);
+  p.Cacc = Cacc;
   p.Cpart = g.splits > 1 ? static_cast<float*>(ws) : nullptr;
   // The fused quantised epilogue needs a whole 128-column group per thread,
   // which the 256-column tile gives; otherwise the codes come from the
@@ -420,14 +466,14 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   }
   if (s != BFP8_OK) return s;
   if (g.splits == 1) {
-    if (Cq == nullptr || fused_here) return BFP8_OK;
+    if (Cq == nullptr || fused_here) return BFP8_OK;  // (Cacc: added by the epilogue)
     QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns, 0u, 0u};
     return launch_quant(qp, false, false, stream);
   }
   const int64_t groups = M * (N / 128);
   const int rgrid = static_cast<int>(std::min<int64_t>((groups + 7) / 8, int64_t(dev->sms) * 16));
   splitk_reduce_kernel<<<rgrid, 256, 0, stream>>>(static_cast<const float*>(ws), g.splits, p.M, p.N,
-                                                   static_cast<uint16_t*>(C), Cq, sCq);
+                                                   static_cast<uint16_t*>(C), Cq, sCq, Cacc);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -606,6 +652,14 @@ bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout, const uint8_t* A, const floa
                    reinterpret_cast<cudaStream_t>(stream));
 }
 
+bfp8_status bfp8_fp8_block_gemm_accumulate(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B,
+                                           const float* sb, int64_t M, int64_t N, int64_t K, float* C_f32, void* ws,
+                                           size_t ws_bytes, bfp8_stream_t stream) {
+  if (C_f32 == nullptr) return BFP8_EINVAL;
+  return gemm_impl(layout, A, sa, B, sb, M, N, K, nullptr, nullptr, nullptr, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), C_f32);
+}
+
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K) {
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return 0;
   return plan_gemm(layout, M, N, K, current_state()).ws_bytes;
@@ -650,10 +704,12 @@ bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, 
   return bfp8_linear_fwd_ex(X, W, M, N, K, Y, WqT, sW, XqT, sXT, ws, ws_bytes, BFP8_SCALE_AMAX448, stream);
 }
 
-bfp8_status bfp8_linear_bwd_ex(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT,
-                               const float* sXT, int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws,
-                               size_t ws_bytes, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
-  if (!dY || !WqT || !sW || !XqT || !sXT || !dX || !dW) return BFP8_EINVAL;
+// The backward pass; dW bf16 is written, or (dW null) the weight gradient
+// is added into the fp32 dW_main.
+static bfp8_status linear_bwd_impl(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT, const float* sXT,
+                            int64_t M, int64_t N, int64_t K, void* dX, void* dW, float* dW_main, void* ws,
+                            size_t ws_bytes, int scale_mode, bfp8_stream_t stream) {
+  if (!dY || !WqT || !sW || !XqT || !sXT || !dX || ((dW == nullptr) == (dW_main == nullptr))) return BFP8_EINVAL;
   if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
   if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
   DeviceState* dev = nullptr;
@@ -672,7 +728,21 @@ bfp8_status bfp8_linear_bwd_ex(const void* dY, const uint8_t* WqT, const float* 
   if ((s = quant_act_impl(dY, M, N, dYq, sdY, dYqT, sdYT, scale_mode, st)) != BFP8_OK) return s;
   if ((s = gemm_impl(BFP8_DGRAD, dYq, sdY, WqT, sW, M, K, N, dX, nullptr, nullptr, gws, gws_bytes, st)) != BFP8_OK)
     return s;
-  return gemm_impl(BFP8_WGRAD, dYqT, sdYT, XqT, sXT, N, K, M, dW, nullptr, nullptr, gws, gws_bytes, st);
+  return gemm_impl(BFP8_WGRAD, dYqT, sdYT, XqT, sXT, N, K, M, dW, nullptr, nullptr, gws, gws_bytes, st, dW_main);
+}
+
+bfp8_status bfp8_linear_bwd_ex(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT,
+                               const float* sXT, int64_t M, int64_t N, int64_t K, void* dX, void* dW, void* ws,
+                               size_t ws_bytes, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  if (dW == nullptr) return BFP8_EINVAL;
+  return linear_bwd_impl(dY, WqT, sW, XqT, sXT, M, N, K, dX, dW, nullptr, ws, ws_bytes, scale_mode, stream);
+}
+
+bfp8_status bfp8_linear_bwd_main_grad(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT,
+                                      const float* sXT, int64_t M, int64_t N, int64_t K, void* dX, float* dW_main,
+                                      void* ws, size_t ws_bytes, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  if (dW_main == nullptr) return BFP8_EINVAL;
+  return linear_bwd_impl(dY, WqT, sW, XqT, sXT, M, N, K, dX, nullptr, dW_main, ws, ws_bytes, scale_mode, stream);
 }
 
 bfp8_status bfp8_linear_bwd(const void* dY, const uint8_t* WqT, const float* sW, const uint8_t* XqT, const float* sXT,

@@ -114,6 +114,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, 
                : "memory");
 }
 
+// 2-D tensor reduce-add shared -> global (TMA): each element of the box is
+// added into the global tensor (type from the tensor map), tracked by bulk
+// groups.
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* src, int32_t c0, int32_t c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   tmap),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until at most N committed bulk groups still read shared memory.

@@ -36,6 +36,13 @@
 
 namespace bfp8 {
 
+// What the epilogue writes.
+enum EpiKind : int {
+  kEpiPlain = 0,  // bf16 C by TMA stores (or fp32 split-K partials)
+  kEpiCodes = 1,  // bf16 C and its E4M3 codes (one split, BN = 256), direct stores
+  kEpiAccum = 2   // C_f32 += result by TMA reduce-add stores (or fp32 split-K partials)
+};
+
 enum SbMode : int {
   kSbBlock = 0,   // sb [N/128, K/128]: FPROP weight blocks
   kSbBlockT = 1,  // sb [K/128, N/128]: DGRAD weight blocks (transposed use)
@@ -55,6 +62,7 @@ struct GemmParams {
   float* Cpart;                 // fp32 [splits, M, N] (splits > 1)
   uint8_t* Cq;                  // optional E4M3 [M, N] (splits == 1)
   float* sCq;                   // optional [N/128, M]
+  float* Cacc;                  // fp32 [M, N] accumulated into instead of C (kEpiAccum, or the split-K reduction)
   uint64_t wait_ns;
 };
 
@@ -162,7 +170,7 @@ __device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], f
 // of 48 KB), the first CTA of the pair issues the MMAs, whose results land in
 // both CTAs' tensor memory (each CTA its own 128 rows x BN columns), and each
 // CTA promotes and stores its own rows.
-template <int BN, int SBMODE, bool kPair, bool kFused>
+template <int BN, int SBMODE, bool kPair, int kEpi>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                           const GemmParams& p) {
   using L = GemmSmem<BN, kPair>;
@@ -406,7 +414,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if constexpr (kFused) {
+      if constexpr (kEpi == kEpiCodes) {
         // One split, BN = 256, codes requested: bf16 and E4M3 outputs are
         // stored directly (each thread owns whole 128-column groups).
         // bf16 output, 8 columns (16 bytes) per store.
@@ -442,6 +450,32 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             *reinterpret_cast<uint4*>(qrow + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
           }
           p.sCq[static_cast<int64_t>(col0 / 128) * p.M + gm] = g.s;
+        }
+      } else if (kEpi == kEpiAccum && p.splits == 1) {
+        // C_f32 += acc: this warp's 32 rows x kCols fp32 values go through
+        // its staging area in passes of kPass columns (boxes of 32 columns,
+        // 128-byte swizzle), each added into global memory by TMA
+        // reduce-add stores, one fp32 addition per element.
+        constexpr int kPass = L::kCWarpBytes / (32 * 4);  // columns per pass: 64 (BN 256) or 32 (BN 128)
+        uint8_t* stg = smem + L::kCOff + warp * L::kCWarpBytes;
+#pragma unroll
+        for (int ps = 0; ps < kCols / kPass; ++ps) {
+          if (lane == 0) bulk_wait_group_read<0>();  // the staging area has been read
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < kPass / 4; ++i) {
+            const float* a = acc + kPass * ps + 4 * i;
+            *reinterpret_cast<float4*>(stg + (i / 8) * 4096 + lane * 128 + (((i % 8) ^ (lane & 7)) << 4)) =
+                make_float4(a[0], a[1], a[2], a[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int bx = 0; bx < kPass / 32; ++bx)
+              tma_reduce_add_2d(&tmC, stg + bx * 4096, col0 + kPass * ps + 32 * bx, c.m0 + quad * 32);
+            bulk_commit_group();
+          }
         }
       } else if (p.splits == 1) {
         // bf16 output through shared memory and TMA stores: this warp's 32
@@ -494,32 +528,35 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
-// kFused selects the instance with the quantised (E4M3) epilogue.  It is a
-// separate instance so that the plain GEMM holds no division code: the
-// fused epilogue's IEEE division fallbacks would otherwise sit (unused) in
-// every GEMM kernel and take part in its register allocation.
-template <int BN, int SBMODE, bool kFused = false>
+// kEpi selects the epilogue (EpiKind).  Each kind is its own instance so
+// that the plain GEMM holds none of the others' code: the E4M3 epilogue's
+// IEEE division fallbacks, for one, would otherwise sit (unused) in every
+// GEMM kernel and take part in its register allocation.  tmC describes the
+// bf16 output for kEpiPlain and the fp32 output for kEpiAccum.
+template <int BN, int SBMODE, int kEpi = kEpiPlain>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  static_assert(!kFused || BN == 256, "the fused epilogue needs whole 128-column groups per thread");
-  gemm_body<BN, SBMODE, false, kFused>(tmA, tmB, tmC, p);
+  static_assert(kEpi != kEpiCodes || BN == 256, "the E4M3 epilogue needs whole 128-column groups per thread");
+  gemm_body<BN, SBMODE, false, kEpi>(tmA, tmB, tmC, p);
 }
 
 // 256 x 256 output tiles on CTA pairs (clusters of two).
-template <int SBMODE, bool kFused = false>
+template <int SBMODE, int kEpi = kEpiPlain>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     block_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  gemm_body<256, SBMODE, true, kFused>(tmA, tmB, tmC, p);
+  gemm_body<256, SBMODE, true, kEpi>(tmA, tmB, tmC, p);
 }
 
 // Adds the fp32 split-K partials in split order, rounds to bf16 and,
 // optionally, quantises each 128-column group of the bf16 result exactly as
 // the activation quantiser does.  One warp per 128-column group of a row.
+// With Cacc the sum is instead added into the fp32 output (one addition per
+// element) and C, Cq are not written.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int N,
                                                             uint16_t* __restrict__ C, uint8_t* __restrict__ Cq,
-                                                            float* __restrict__ sCq) {
+                                                            float* __restrict__ sCq, float* __restrict__ Cacc) {
   const int64_t groups = static_cast<int64_t>(M) * (N / 128);
   const int lane = threadIdx.x & 31;
   for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; g < groups;
@@ -533,6 +570,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
       a.y += b.y;
       a.z += b.z;
       a.w += b.w;
+    }
+    if (Cacc != nullptr) {
+      float4 m = *reinterpret_cast<const float4*>(Cacc + off);
+      m.x += a.x;
+      m.y += a.y;
+      m.z += a.z;
+      m.w += a.w;
+      *reinterpret_cast<float4*>(Cacc + off) = m;
+      continue;
     }
     const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
     uint2 v;

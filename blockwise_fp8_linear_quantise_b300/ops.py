@@ -144,6 +144,27 @@ def fp8_block_gemm(layout, A, sa, B, sb, C=None, fused_quant=False, Cq=None, sCq
     return (C, Cq, sCq) if fused_quant else C
 
 
+def fp8_block_gemm_accumulate(layout, A, sa, B, sb, C_f32, workspace=None, stream=None):
+    """C_f32 [M, N] (fp32, updated in place) += the block-scaled product of
+    fp8_block_gemm's operands.  Returns C_f32."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, torch.uint8, (M, K), "A")
+    _need(B, torch.uint8, (N, K), "B")
+    _need(sa, torch.float32, (K // 128, M), "sa")
+    sb_shape = {FPROP: (N // 128, K // 128), DGRAD: (K // 128, N // 128), WGRAD: (K // 128, N)}[layout]
+    _need(sb, torch.float32, sb_shape, "sb")
+    _need(C_f32, torch.float32, (M, N), "C_f32")
+    ws_n = gemm_workspace_bytes(layout, M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=A.device)
+    lib = _lib.load()
+    _check(lib.bfp8_fp8_block_gemm_accumulate(layout, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb), M, N, K, _ptr(C_f32),
+                                              _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp8_block_gemm_accumulate")
+    return C_f32
+
+
 def linear_fwd_workspace_bytes(M, N, K):
     return int(_lib.load().bfp8_linear_fwd_workspace_bytes(M, N, K))
 
@@ -176,9 +197,10 @@ def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None, scale_mode
     return Y, saved
 
 
-def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None, scale_mode="amax448"):
+def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None, scale_mode="amax448", dW_main=None):
     """(dX, dW) for the layer whose forward produced ``saved``; scale_mode
-    applies to the quantisation of dY."""
+    applies to the quantisation of dY.  With dW_main (fp32 [N, K]) the weight
+    gradient is added into it instead and (dX, dW_main) is returned."""
     M, N = dY.shape
     K = saved["WqT"].shape[0]
     _need(dY, torch.bfloat16, (M, N), "dY")
@@ -188,10 +210,17 @@ def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None, scale_m
     _need(saved["sXT"], torch.float32, (M // 128, K), "sXT")
     dev = dY.device
     dX = _out(dX, torch.bfloat16, (M, K), dev, "dX")
-    dW = _out(dW, torch.bfloat16, (N, K), dev, "dW")
     if workspace is None:
         workspace = torch.empty(linear_bwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     lib = _lib.load()
+    if dW_main is not None:
+        _need(dW_main, torch.float32, (N, K), "dW_main")
+        _check(lib.bfp8_linear_bwd_main_grad(_ptr(dY), _ptr(saved["WqT"]), _ptr(saved["sW"]), _ptr(saved["XqT"]),
+                                             _ptr(saved["sXT"]), M, N, K, _ptr(dX), _ptr(dW_main), _ptr(workspace),
+                                             workspace.numel(), _scale_mode(scale_mode), _stream(stream)),
+               "linear_bwd_main_grad")
+        return dX, dW_main
+    dW = _out(dW, torch.bfloat16, (N, K), dev, "dW")
     _check(lib.bfp8_linear_bwd_ex(_ptr(dY), _ptr(saved["WqT"]), _ptr(saved["sW"]), _ptr(saved["XqT"]),
                                   _ptr(saved["sXT"]), M, N, K, _ptr(dX), _ptr(dW), _ptr(workspace),
                                   workspace.numel(), _scale_mode(scale_mode), _stream(stream)), "linear_bwd")

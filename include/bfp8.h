@@ -159,6 +159,24 @@ bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout,
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K);
 
 /*
+ * fp32 accumulate-into GEMM: C_f32 [M, N] += the block-scaled product, with
+ * the operands, scales and layouts of bfp8_fp8_block_gemm.  Each element
+ * receives one fp32 addition of the fp32 promotion accumulator (no bf16
+ * rounding), as an fp32 main gradient needs: section 3.2 keeps the training
+ * state on the BF16/FP32 path.  C_f32 is caller-owned, read and written;
+ * calls on the same C_f32 must not overlap.  The workspace is the one
+ * bfp8_gemm_workspace_bytes() reports for the same layout and sizes.
+ * Errors: as bfp8_fp8_block_gemm; C_f32 null returns BFP8_EINVAL.
+ */
+bfp8_status bfp8_fp8_block_gemm_accumulate(bfp8_layout layout,
+                                           const uint8_t* A, const float* sa,
+                                           const uint8_t* B, const float* sb,
+                                           int64_t M, int64_t N, int64_t K,
+                                           float* C_f32,
+                                           void* workspace, size_t ws_bytes,
+                                           bfp8_stream_t stream);
+
+/*
  * The same GEMM as bfp8_fp8_block_gemm, for callers that cannot allocate
  * device memory: code that runs where cudaMalloc is not allowed or not
  * wanted (inside a host callback, a custom allocator, a real-time loop
@@ -250,6 +268,20 @@ bfp8_status bfp8_linear_bwd_ex(const void* dY,
                                void* dX, void* dW,
                                void* ws, size_t ws_bytes,
                                bfp8_scale_mode scale_mode, bfp8_stream_t stream);
+
+/*
+ * bfp8_linear_bwd_ex with the weight gradient added into an fp32 main
+ * gradient instead of written as bf16: dW_main [N, K] fp32 (caller-owned,
+ * read and written) += dY^T . X by bfp8_fp8_block_gemm_accumulate.  dX is
+ * bf16 as before; workspace and errors as bfp8_linear_bwd.
+ */
+bfp8_status bfp8_linear_bwd_main_grad(const void* dY,
+                                      const uint8_t* WqT, const float* sW,
+                                      const uint8_t* XqT, const float* sXT,
+                                      int64_t M, int64_t N, int64_t K,
+                                      void* dX, float* dW_main,
+                                      void* ws, size_t ws_bytes,
+                                      bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

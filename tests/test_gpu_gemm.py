@@ -213,3 +213,80 @@ def test_full_stack_gate_up_layer():
     run_layouts(o, ["dgrad"], r, c)
     r, c = sampled(N, K, 10)
     run_layouts(o, ["wgrad"], r, c)
+
+
+# ------------------------------------------------------- fp32 accumulate-into
+
+
+def _accumulate(o, lay, C):
+    if lay == "fprop":
+        ops.fp8_block_gemm_accumulate(ops.FPROP, gpu(o, "Xq"), gpu(o, "sX"), gpu(o, "Wq"), gpu(o, "sW"), C)
+        return ogemm.fprop(o["Xq"], o["sX"], o["Wq"], o["sW"])[0]
+    if lay == "dgrad":
+        ops.fp8_block_gemm_accumulate(ops.DGRAD, gpu(o, "dYq"), gpu(o, "sdY"), gpu(o, "WqT"), gpu(o, "sW"), C)
+        return ogemm.dgrad(o["dYq"], o["sdY"], o["WqT"], o["sW"])[0]
+    ops.fp8_block_gemm_accumulate(ops.WGRAD, gpu(o, "dYqT"), gpu(o, "sdYT"), gpu(o, "XqT"), gpu(o, "sXT"), C)
+    return ogemm.wgrad(o["dYqT"], o["sdYT"], o["XqT"], o["sXT"])[0]
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 640), (256, 384, 1280)])
+def test_accumulate_into_fp32_all_layouts(M, N, K, splits, gemm_kind):
+    """C_f32 += product, twice: each increment is the oracle's fp32
+    accumulator within the GEMM tolerance, and the untouched start values
+    survive exactly where the product is zero (none here) or are changed by
+    one fp32 addition (checked through the increment)."""
+    X, W, dY = rand_layer(M, N, K, M + 3 * N + K)
+    o = quantised_layer(X, W, dY)
+    rng = np.random.default_rng(11)
+    try:
+        ops.set_gemm_splits(splits)
+        for lay in ("fprop", "dgrad", "wgrad"):
+            shape = {"fprop": (M, N), "dgrad": (M, K), "wgrad": (N, K)}[lay]
+            C0 = torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(dev())
+            C = C0.clone()
+            acc = _accumulate(o, lay, C)
+            assert ops.sync_status() == 0
+            scale = np.abs(acc).max()
+            C0s = C0 * float(scale)  # start values of the accumulator's size
+            C = C0s.clone()
+            _accumulate(o, lay, C)
+            assert ops.sync_status() == 0
+            inc1 = (C.double() - C0s.double()).cpu().numpy()
+            assert rel_fro(inc1, acc) <= REL_FRO_TOL, (lay, rel_fro(inc1, acc))
+            _accumulate(o, lay, C)
+            assert ops.sync_status() == 0
+            inc2 = (C.double() - C0s.double()).cpu().numpy()
+            assert rel_fro(inc2, 2.0 * acc) <= REL_FRO_TOL, lay
+            # the plain GEMM's bf16 output rounds the same accumulator
+            Cb = run_layouts(o, [lay])[lay][0]
+            assert rel_fro(np32(Cb), inc1) <= 1e-2
+    finally:
+        ops.set_gemm_splits(0)
+
+
+def test_linear_bwd_main_grad_matches_oracle():
+    X, W, dY = rand_layer(384, 512, 640, 21)
+    Xg, Wg, dYg = (workloads.to_bf16(a).to(dev()) for a in (X, W, dY))
+    _, saved = ops.linear_fwd(Xg, Wg)
+    dX_ref, dW_ref = ops.linear_bwd(dYg, saved)
+    main0 = np.random.default_rng(5).standard_normal((512, 640)).astype(np.float32) * 1e-3
+    main = torch.from_numpy(main0).to(dev())
+    dX, main1 = ops.linear_bwd(dYg, saved, dW_main=main)
+    assert ops.sync_status() == 0
+    assert main1.data_ptr() == main.data_ptr()
+    assert torch.equal(dX, dX_ref)
+    _, o_saved = ogemm.linear_fwd(X, W)
+    _, want = ogemm.linear_bwd(dY, o_saved, main_grad=main0)
+    got_inc = (main1.double().cpu().numpy() - main0)
+    want_inc = want.astype(np.float64) - main0
+    assert rel_fro(got_inc, want_inc) <= REL_FRO_TOL
+    assert rel_fro(np32(dW_ref), got_inc) <= 1e-2
+
+
+def test_accumulate_rejects_a_missing_target():
+    from blockwise_fp8_linear_quantise_b300 import _lib
+    st = torch.cuda.current_stream().cuda_stream
+    fake = 1 << 20
+    assert _lib.load().bfp8_fp8_block_gemm_accumulate(ops.FPROP, fake, fake, fake, fake, 256, 256, 256, None,
+                                                      None, 0, st) == 1
