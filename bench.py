@@ -88,6 +88,10 @@ def parse_args(argv=None):
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
     ap.add_argument("--scale-mode", choices=["amax448", "pow2"], default="amax448",
                     help="group scale rule: amax/448 (default) or the power-of-two mode")
+    ap.add_argument("--main-grad", action="store_true",
+                    help="WGRAD adds into fp32 main gradients (bfp8_fp8_block_gemm_accumulate) instead of bf16 dW")
+    ap.add_argument("--cached-weights", action="store_true",
+                    help="weights quantised once before the timed steps (cached across micro-steps)")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
     return ap.parse_args(argv)
@@ -158,8 +162,10 @@ def gemm_flops(specs):
     return sum(2 * s.M * s.N * s.K * (3 if s.backward else 1) for s in specs)
 
 
-def workload_config(wl, specs, layers, scale_mode="amax448"):
+def workload_config(wl, specs, layers, scale_mode="amax448", main_grad=False, cached_weights=False):
     cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M, "scale_mode": scale_mode,
+           "dW": "fp32 main-grad accumulate" if main_grad else "bf16",
+           "weights": "quantised once (cached)" if cached_weights else "quantised every step",
            "shapes_MNK": sorted({(s.M, s.N, s.K) for s in specs}),
            "passes": "fprop+dgrad+wgrad" if specs[0].backward else "fprop",
            "l2": "inputs larger than L2: each step streams several GB through HBM (no explicit flush)",
@@ -315,7 +321,7 @@ class StackRunner:
     a step only makes the ctypes calls.
     """
 
-    def __init__(self, wl, specs, dev, scale_mode="amax448"):
+    def __init__(self, wl, specs, dev, scale_mode="amax448", main_grad=False, cached_weights=False):
         import torch
         from blockwise_fp8_linear_quantise_b300 import _lib, ops, workloads
         self.torch = torch
@@ -323,6 +329,8 @@ class StackRunner:
         self.ops = ops
         self.scale_mode = scale_mode
         self.mode_id = ops.SCALE_MODES[scale_mode]
+        self.main_grad = main_grad            # WGRAD adds into fp32 main gradients
+        self.cached_weights = cached_weights  # weights quantised once, before any step
         self.specs = specs
         self.dev = dev
         u8, f32, bf16 = torch.uint8, torch.float32, torch.bfloat16
@@ -353,7 +361,12 @@ class StackRunner:
                                          dYqT=E((N, M), u8), sdYT=E((M // 128, N), f32), dX=E((M, K), bf16))
             self.saved.append(dict(WqT=E((K, N), u8), sW=E((N // 128, K // 128), f32),
                                    XqT=E((K, M), u8), sXT=E((M // 128, K), f32)))
-            self.dW.append(E((N, K), bf16) if s.backward else None)
+            if cached_weights:
+                self.saved[-1]["Wq"] = E((N, K), u8)
+            if s.backward:
+                self.dW.append(torch.zeros((N, K), dtype=f32, device=dev) if main_grad else E((N, K), bf16))
+            else:
+                self.dW.append(None)
             ws = max(ws, ops.gemm_workspace_bytes(ops.FPROP, M, N, K))
             if s.backward:
                 ws = max(ws, ops.gemm_workspace_bytes(ops.DGRAD, M, K, N),
@@ -362,6 +375,11 @@ class StackRunner:
             ws = max(ws, ops.linear_fwd_workspace_bytes(M, N, K))
         self.ws = E((max(ws, 256),), u8)
         self.ws_bytes = self.ws.numel()
+        if cached_weights:  # once per optimizer step, outside the timed micro-steps
+            for i, s in enumerate(specs):
+                sv = self.saved[i]
+                ops.quantize_w_128x128(self.inputs[(s.w_tag, workloads.layer_of(s))], q=sv["Wq"], qT=sv["WqT"],
+                                       s=sv["sW"], scale_mode=scale_mode)
         self._marshal()
 
     def _marshal(self):
@@ -377,12 +395,14 @@ class StackRunner:
             from blockwise_fp8_linear_quantise_b300 import workloads
             W = self.inputs[(s.w_tag, workloads.layer_of(s))]
             ne_w, ne_x = N * K, M * K
-            fwd.append(("quant_w", ne_w * (4 + 4 / 16384), lib.bfp8_quantize_w_128x128_ex,
-                        (P(W), N, K, P(sc["Wq"]), P(sv["WqT"]), P(sv["sW"]), self.mode_id)))
+            Wq = sv["Wq"] if self.cached_weights else sc["Wq"]
+            if not self.cached_weights:
+                fwd.append(("quant_w", ne_w * (4 + 4 / 16384), lib.bfp8_quantize_w_128x128_ex,
+                            (P(W), N, K, P(Wq), P(sv["WqT"]), P(sv["sW"]), self.mode_id)))
             fwd.append(("quant_act", ne_x * (4 + 8 / 128), lib.bfp8_quantize_act_1x128_ex,
                         (P(X), M, K, P(sc["Xq"]), P(sc["sX"]), P(sv["XqT"]), P(sv["sXT"]), self.mode_id)))
             fwd.append(("fprop", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
-                        (self.ops.FPROP, P(sc["Xq"]), P(sc["sX"]), P(sc["Wq"]), P(sv["sW"]), M, N, K, P(sc["Y"]),
+                        (self.ops.FPROP, P(sc["Xq"]), P(sc["sX"]), P(Wq), P(sv["sW"]), M, N, K, P(sc["Y"]),
                          None, None, P(self.ws), self.ws_bytes)))
             if s.backward:
                 dY = self.inputs[(s.dy_tag, None)]
@@ -392,6 +412,9 @@ class StackRunner:
                      ("dgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
                       (self.ops.DGRAD, P(sc["dYq"]), P(sc["sdY"]), P(sv["WqT"]), P(sv["sW"]), M, K, N, P(sc["dX"]),
                        None, None, P(self.ws), self.ws_bytes)),
+                     ("wgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm_accumulate,
+                      (self.ops.WGRAD, P(sc["dYqT"]), P(sc["sdYT"]), P(sv["XqT"]), P(sv["sXT"]), N, K, M,
+                       P(self.dW[i]), P(self.ws), self.ws_bytes)) if self.main_grad else
                      ("wgrad", 2.0 * M * N * K, lib.bfp8_fp8_block_gemm,
                       (self.ops.WGRAD, P(sc["dYqT"]), P(sc["sdYT"]), P(sv["XqT"]), P(sv["sXT"]), N, K, M,
                        P(self.dW[i]), None, None, P(self.ws), self.ws_bytes))]
@@ -534,7 +557,7 @@ def gpu_arm(args):
     wl = workloads.make(args.workload)
     layers = args.layers if args.workload == "stack28" else 0
     specs = linear_list(wl, layers)
-    runner = StackRunner(wl, specs, dev, args.scale_mode)
+    runner = StackRunner(wl, specs, dev, args.scale_mode, args.main_grad, args.cached_weights)
     flops_step = gemm_flops(specs)
 
     # warm-up
@@ -606,7 +629,10 @@ def gpu_arm(args):
 
     # e2e through the public fused calls with host buffers
     e2e = None
-    if not args.no_e2e:
+    if args.main_grad or args.cached_weights:
+        e2e = {"value": None, "unit": UNIT,
+               "skipped": "measured for the default step only (fused linear_fwd / linear_bwd with bf16 dW)"}
+    elif not args.no_e2e:
         runner.e2e_setup()
         for _ in range(max(1, min(args.warmup, 2))):
             runner.e2e_step()
@@ -645,7 +671,7 @@ def gpu_arm(args):
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
-                "data": "synthetic", "config": workload_config(wl, specs, layers, args.scale_mode),
+                "data": "synthetic", "config": workload_config(wl, specs, layers, args.scale_mode, args.main_grad, args.cached_weights),
                 "roofline": roofline, "roofline_quant": roofline_q, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk, "per_kernel": per_kernel,
                 "gemm_tflop_per_step": flops_step / 1e12, "kernel_source": src_hash}

@@ -25,6 +25,8 @@ SIGNATURES = {
     "bfp8_linear_fwd_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "bfp8_linear_bwd": (c_int, [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_sz, c_p]),
     "bfp8_linear_bwd_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64]),
+    "bfp8_linear_fwd_prequantised": (c_int, [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_sz, c_int,
+                                             c_p]),
     "bfp8_linear_fwd_ex": (c_int, [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_int, c_p]),
     "bfp8_linear_bwd_ex": (c_int, [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_sz, c_int, c_p]),
     "bfp8_linear_bwd_main_grad": (c_int, [c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_sz, c_int,

@@ -699,6 +699,29 @@ bfp8_status bfp8_linear_fwd_ex(const void* X, const void* W, int64_t M, int64_t 
   return gemm_impl(BFP8_FPROP, Xq, sX, Wq, sW, M, N, K, Y, nullptr, nullptr, gws, gws_bytes, st);
 }
 
+bfp8_status bfp8_linear_fwd_prequantised(const void* X, const uint8_t* Wq, const float* sW, int64_t M, int64_t N,
+                                         int64_t K, void* Y, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes,
+                                         bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  if (!X || !Wq || !sW || !Y || !XqT || !sXT) return BFP8_EINVAL;
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  const size_t need = fwd_ws(M, N, K, *dev, nullptr, nullptr, nullptr, nullptr, nullptr);
+  if (ws == nullptr || ws_bytes < need) return BFP8_EWORKSPACE;
+  if (!aligned16(ws)) return BFP8_EALIGN;
+  Carver cv(ws);
+  uint8_t* Xq;
+  float* sX;
+  void* gws;
+  fwd_ws(M, N, K, *dev, &cv, nullptr, &Xq, &sX, &gws);  // the weight-code region stays unused
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = quant_act_impl(X, M, K, Xq, sX, XqT, sXT, scale_mode, st)) != BFP8_OK) return s;
+  const size_t gws_bytes = ws_bytes - (static_cast<uint8_t*>(gws) - static_cast<uint8_t*>(ws));
+  return gemm_impl(BFP8_FPROP, Xq, sX, Wq, sW, M, N, K, Y, nullptr, nullptr, gws, gws_bytes, st);
+}
+
 bfp8_status bfp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K, void* Y, uint8_t* WqT,
                             float* sW, uint8_t* XqT, float* sXT, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
   return bfp8_linear_fwd_ex(X, W, M, N, K, Y, WqT, sW, XqT, sXT, ws, ws_bytes, BFP8_SCALE_AMAX448, stream);

@@ -197,6 +197,34 @@ def linear_fwd(X, W, Y=None, saved=None, workspace=None, stream=None, scale_mode
     return Y, saved
 
 
+def linear_fwd_prequantised(X, Wq, sW, WqT=None, Y=None, saved=None, workspace=None, stream=None,
+                            scale_mode="amax448"):
+    """Y = X . W^T with W's codes Wq [N, K] and scales sW [N/128, K/128]
+    quantised earlier (quantize_w_128x128), e.g. once per optimizer step.
+    Returns (Y, saved) like linear_fwd; saved takes WqT (when given) and sW
+    for linear_bwd."""
+    M, K = X.shape
+    N = Wq.shape[0]
+    _need(X, torch.bfloat16, (M, K), "X")
+    _need(Wq, torch.uint8, (N, K), "Wq")
+    _need(sW, torch.float32, (N // 128, K // 128), "sW")
+    dev = X.device
+    Y = _out(Y, torch.bfloat16, (M, N), dev, "Y")
+    if saved is None:
+        saved = dict(XqT=torch.empty((K, M), dtype=torch.uint8, device=dev),
+                     sXT=torch.empty((M // 128, K), dtype=torch.float32, device=dev))
+    saved["sW"] = sW
+    if WqT is not None:
+        saved["WqT"] = WqT
+    if workspace is None:
+        workspace = torch.empty(linear_fwd_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    lib = _lib.load()
+    _check(lib.bfp8_linear_fwd_prequantised(_ptr(X), _ptr(Wq), _ptr(sW), M, N, K, _ptr(Y), _ptr(saved["XqT"]),
+                                            _ptr(saved["sXT"]), _ptr(workspace), workspace.numel(),
+                                            _scale_mode(scale_mode), _stream(stream)), "linear_fwd_prequantised")
+    return Y, saved
+
+
 def linear_bwd(dY, saved, dX=None, dW=None, workspace=None, stream=None, scale_mode="amax448", dW_main=None):
     """(dX, dW) for the layer whose forward produced ``saved``; scale_mode
     applies to the quantisation of dY.  With dW_main (fp32 [N, K]) the weight

@@ -248,6 +248,23 @@ bfp8_status bfp8_linear_bwd(const void* dY,
 size_t bfp8_linear_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
+ * Forward of one linear layer whose weight is already quantised: the
+ * weight quantisation cached across micro-steps (W changes only at an
+ * optimizer step, while section 3.2 re-quantises it on every use).  Wq E4M3
+ * [N, K] and sW fp32 [N/128, K/128] are what bfp8_quantize_w_128x128 (or
+ * _ex) returned for the current W; its WqT serves bfp8_linear_bwd.  Runs the
+ * dual activation quantiser (scale_mode) and the FPROP GEMM.  X, Y, XqT,
+ * sXT, the workspace (bfp8_linear_fwd_workspace_bytes) and errors are those
+ * of bfp8_linear_fwd; Y equals bfp8_linear_fwd's output bit for bit when Wq
+ * and sW come from the same W.
+ */
+bfp8_status bfp8_linear_fwd_prequantised(const void* X, const uint8_t* Wq, const float* sW,
+                                         int64_t M, int64_t N, int64_t K,
+                                         void* Y, uint8_t* XqT, float* sXT,
+                                         void* ws, size_t ws_bytes,
+                                         bfp8_scale_mode scale_mode, bfp8_stream_t stream);
+
+/*
  * bfp8_linear_fwd / bfp8_linear_bwd with an explicit scale rule for every
  * quantisation they run (see bfp8_quantize_act_1x128_ex).  The saved tensors
  * carry fp32 scales in either mode; bfp8_linear_bwd_ex takes the mode for

@@ -50,3 +50,25 @@ def test_linear_repeat_is_deterministic():
         outs.append((Y.clone(), dX.clone(), dW.clone()))
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+def test_prequantised_weights_give_the_same_forward(scale_mode):
+    """Weights quantised once (cached across micro-steps) and passed to the
+    prequantised forward give linear_fwd's output and saved tensors bit for
+    bit; the backward runs from them unchanged."""
+    rng = np.random.default_rng(31)
+    X = workloads.to_bf16(rng.standard_normal((512, 384)).astype(np.float32)).to(dev())
+    W = workloads.to_bf16((rng.standard_normal((640, 384)) * 0.02).astype(np.float32)).to(dev())
+    dY = workloads.to_bf16((rng.standard_normal((512, 640)) * 1e-3).astype(np.float32)).to(dev())
+    Y, saved = ops.linear_fwd(X, W, scale_mode=scale_mode)
+    Wq, WqT, sW = ops.quantize_w_128x128(W, scale_mode=scale_mode)
+    for _ in range(2):  # the cached weight serves several micro-steps
+        Y2, saved2 = ops.linear_fwd_prequantised(X, Wq, sW, WqT=WqT, scale_mode=scale_mode)
+        assert ops.sync_status() == 0
+        assert torch.equal(Y2, Y)
+        for k in ("WqT", "sW", "XqT", "sXT"):
+            assert torch.equal(saved2[k], saved[k]), k
+    dX, dW = ops.linear_bwd(dY, saved, scale_mode=scale_mode)
+    dX2, dW2 = ops.linear_bwd(dY, saved2, scale_mode=scale_mode)
+    assert torch.equal(dX, dX2) and torch.equal(dW, dW2)
