@@ -92,6 +92,8 @@ def parse_args(argv=None):
                     help="WGRAD adds into fp32 main gradients (bfp8_fp8_block_gemm_accumulate) instead of bf16 dW")
     ap.add_argument("--cached-weights", action="store_true",
                     help="weights quantised once before the timed steps (cached across micro-steps)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as replays of a CUDA graph captured once (per-call rates from an eager pass)")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
     return ap.parse_args(argv)
@@ -162,8 +164,9 @@ def gemm_flops(specs):
     return sum(2 * s.M * s.N * s.K * (3 if s.backward else 1) for s in specs)
 
 
-def workload_config(wl, specs, layers, scale_mode="amax448", main_grad=False, cached_weights=False):
+def workload_config(wl, specs, layers, scale_mode="amax448", main_grad=False, cached_weights=False, graph=False):
     cfg = {"workload": wl.name, "linears": len(specs), "tokens": specs[0].M, "scale_mode": scale_mode,
+           "launch": "CUDA-graph replay" if graph else "eager ABI calls",
            "dW": "fp32 main-grad accumulate" if main_grad else "bf16",
            "weights": "quantised once (cached)" if cached_weights else "quantised every step",
            "shapes_MNK": sorted({(s.M, s.N, s.K) for s in specs}),
@@ -567,6 +570,24 @@ def gpu_arm(args):
     if ops.sync_status() != 0:
         raise SystemExit("device status not ok after warm-up")
 
+    # --graph: the step's calls are captured once into a CUDA graph, and the
+    # timed region replays it (no host work per launch)
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            runner.step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        n0 = ops.launch_count()
+        with torch.cuda.graph(graph):
+            runner.step()
+        graph_launches = ops.launch_count() - n0
+        graph.replay()
+        torch.cuda.synchronize()
+
     # timed region
     clocks = ClockSampler(gpu_uuid(dev))
     barrier(group)
@@ -578,15 +599,23 @@ def gpu_arm(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
     for _ in range(args.steps):
-        runner.step(marks)
+        if graph is not None:
+            graph.replay()
+        else:
+            runner.step(marks)
     t_end.record()
     torch.cuda.synchronize()
-    launches = ops.launch_count() - launches0
+    launches = ops.launch_count() - launches0 if graph is None else graph_launches * args.steps
     clk = clocks.stop()
     barrier(group)
     st = ops.sync_status()
     if st != 0:
         raise SystemExit(f"device status {st} in the timed region")
+    if graph is not None:
+        # per-call durations come from an eager pass of the same steps
+        for _ in range(args.steps):
+            runner.step(marks)
+        torch.cuda.synchronize()
     ms_local = t_start.elapsed_time(t_end)
     ms = max_over_ranks(ms_local, group)
     total_flops = sum_over_ranks(flops_step * args.steps, group)
@@ -671,7 +700,8 @@ def gpu_arm(args):
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)",
-                "data": "synthetic", "config": workload_config(wl, specs, layers, args.scale_mode, args.main_grad, args.cached_weights),
+                "data": "synthetic", "config": workload_config(wl, specs, layers, args.scale_mode, args.main_grad, args.cached_weights,
+                                          args.graph),
                 "roofline": roofline, "roofline_quant": roofline_q, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk, "per_kernel": per_kernel,
                 "gemm_tflop_per_step": flops_step / 1e12, "kernel_source": src_hash}
