@@ -57,18 +57,46 @@ FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
 # averaged over the launches of one stack layer (the same 24 launches as
 # every layer of the step), from an ncu capture of
 #   python bench.py --layers 1 --steps 1 --warmup 0 --no-e2e --no-cpu-baseline
-# Valid only for the kernel sources whose hash is the key; once the kernels
-# change the bench line reports null until a new capture is recorded.
+# Valid only for the kernel code whose hash (comments ignored) is the key;
+# once the kernels change the bench line reports null until a new capture is
+# recorded.
 TRAFFIC = {
-    "fb42219e88203ef8": {"gemm": 231.3e6, "quant": 155.2e6},
+    "09a083e2700dba3b": {"gemm": 231.3e6, "quant": 155.2e6},
 }
 
 
+def strip_comments(src):
+    """C/C++ source without // and /* */ comments and with whitespace
+    collapsed, so that an edit of comments alone leaves the hash unchanged.
+    String and character literals are kept verbatim."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash():
+    """Hash of the kernel sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
     for f in ("common.cuh", "gemm.cuh", "quant.cuh", "api.cu"):
-        with open(os.path.join(ROOT, "blockwise_fp8_linear_quantise_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "blockwise_fp8_linear_quantise_b300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

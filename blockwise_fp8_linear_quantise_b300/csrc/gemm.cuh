@@ -11,22 +11,29 @@
 // elements) cannot express, so every slice's partial product leaves the
 // tensor core and is promoted in fp32 by CUDA cores:
 //
-//   warp 8      TMA producer: per slice, a 128x128 A tile and a BNx128 B tile
-//               (both 128-byte swizzled) into a STAGES-deep shared-memory ring.
+//   warp 8      producer: per slice, lane 0 loads a 128x128 A tile and a
+//               BNx128 B tile (both 128-byte swizzled, TMA) into a
+//               STAGES-deep shared-memory ring, and all 32 lanes copy the
+//               slice's scales (sa of the CTA's rows, sb) into an 8-slot
+//               scale ring with cp.async, so no promotion warp ever waits on
+//               a global load.
 //   warp 9      MMA issuer: 4 x tcgen05.mma (K=32 each) write the slice's
 //               partial P_kb into one of two TMEM buffers (BN fp32 columns
 //               each); commits release the smem stage and signal the buffer.
 //   warps 0..7  promotion: warp w reads TMEM lanes 32*(w%4).. (its 32 rows)
 //               and columns 128*(w/4).. of the buffer, multiplies by the
-//               slice's scale product and adds into 128 fp32 accumulators
-//               per thread held in registers, then frees the buffer.  While
-//               they promote slice kb the tensor core already computes kb+1.
-//               At the end of a tile they convert to bf16 and hand the
-//               tile to TMA stores through shared memory (or, with the
-//               fused E4M3 epilogue or split-K, store directly).
+//               slice's scale product (from the scale ring) and adds into
+//               128 fp32 accumulators per thread held in registers, then
+//               frees the buffer.  While they promote slice kb the tensor
+//               core already computes kb+1.  At the end of a tile the
+//               epilogue (EpiKind) converts to bf16 and hands the tile to TMA
+//               stores through shared memory, adds it into an fp32 output by
+//               TMA reduce-add stores, or (E4M3 codes, split-K partials)
+//               stores directly.
 //
-// The kernel is persistent: one CTA per SM walks work units (tile, split)
-// in a grouped order that keeps a band of A rows and B rows hot in L2.
+// The kernel is persistent: one CTA (or CTA pair, 256 x 256 tiles with
+// tcgen05 cta_group::2 MMAs) per SM walks work units (tile, split) in a
+// grouped order that keeps a band of A rows and B rows hot in L2.
 // With split-K, each split writes fp32 partial sums to a workspace and a
 // separate kernel adds them in a fixed order (deterministic).
 #pragma once
