@@ -233,9 +233,7 @@ def _accumulate(o, lay, C):
 @pytest.mark.parametrize("M,N,K", [(512, 768, 640), (256, 384, 1280)])
 def test_accumulate_into_fp32_all_layouts(M, N, K, splits, gemm_kind):
     """C_f32 += product, twice: each increment is the oracle's fp32
-    accumulator within the GEMM tolerance, and the untouched start values
-    survive exactly where the product is zero (none here) or are changed by
-    one fp32 addition (checked through the increment)."""
+    accumulator (before bf16 rounding) within the GEMM tolerance."""
     X, W, dY = rand_layer(M, N, K, M + 3 * N + K)
     o = quantised_layer(X, W, dY)
     rng = np.random.default_rng(11)
@@ -290,3 +288,22 @@ def test_accumulate_rejects_a_missing_target():
     fake = 1 << 20
     assert _lib.load().bfp8_fp8_block_gemm_accumulate(ops.FPROP, fake, fake, fake, fake, 256, 256, 256, None,
                                                       None, 0, st) == 1
+
+
+def test_full_stack_gate_up_wgrad_accumulate():
+    """fp32 main-gradient accumulation at the stack's largest WGRAD
+    (12288 x 2048 over 16384 tokens), checked on sampled outputs."""
+    wl = workloads.make("stack28")
+    X = np32(workloads.tensor(wl, "x_h"))
+    dY = np32(workloads.tensor(wl, "dy_gu"))
+    o = quantised_layer(X, None, dY)
+    N, K = dY.shape[1], X.shape[1]
+    r, c = sampled(N, K, 12)
+    want = ogemm.wgrad(o["dYqT"], o["sdYT"], o["XqT"], o["sXT"], rows=r, cols=c)[0]
+    rng = np.random.default_rng(13)
+    C0 = torch.from_numpy((rng.standard_normal((N, K)) * float(np.abs(want).max())).astype(np.float32)).to(dev())
+    C = C0.clone()
+    ops.fp8_block_gemm_accumulate(ops.WGRAD, gpu(o, "dYqT"), gpu(o, "sdYT"), gpu(o, "XqT"), gpu(o, "sXT"), C)
+    assert ops.sync_status() == 0
+    inc = (C.double() - C0.double()).cpu().numpy()[np.ix_(r, c)]
+    assert rel_fro(inc, want) <= REL_FRO_TOL
