@@ -30,6 +30,17 @@ saturates and the largest lands in (224, 448]; an all-zero group keeps
 s = 1.  Step 3 is unchanged: x/s with s a power of two is an exact scaling
 (rounded once only where it leaves the fp32 range).
 
+Reciprocal-multiply mode (scale_mode="mul_recip").  The pages do not say
+whether a code comes from dividing by the scale or from multiplying by its
+reciprocal; this mode takes the second reading.  The stored scale is the
+default mode's s = float32(amax / 448), so the GEMMs consume it unchanged,
+and each group's codes are q = E4M3_rn_satfinite(float32(x * m)) with one
+multiplier per group, m = float32(448 / amax) (one IEEE division per group,
+none per element).  m saturates at the largest finite float32, which only a
+group with amax below 448 / FLT_MAX (about 2^-119.2) reaches; an all-zero
+group gets m = 1.  The two roundings (of m, then of x * m) make some codes
+one E4M3 step away from the default mode's, near the E4M3 rounding midpoints.
+
 Scale layouts (shared with the C ABI, which states the same contract):
 
 * quantize_act_1x128(X [R, C]) groups along C:  q [R, C],  s [C/128, R]
@@ -85,7 +96,19 @@ def group_scale_pow2(amax):
     return np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
 
 
-SCALE_MODES = {"amax448": group_scale, "pow2": group_scale_pow2}
+def group_multiplier(amax):
+    """Code multiplier of the reciprocal-multiply mode: float32(448 / amax) by
+    one IEEE float32 division, saturated at the largest finite float32; 1 when
+    amax == 0."""
+    amax = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        m = E4M3_MAX / amax  # float32 / float32 -> float32, IEEE round to nearest
+    m = np.minimum(m, np.finfo(np.float32).max)
+    return np.where(amax == 0, np.float32(1.0), m).astype(np.float32)
+
+
+# the stored (dequantisation) scale of each mode
+SCALE_MODES = {"amax448": group_scale, "pow2": group_scale_pow2, "mul_recip": group_scale}
 
 
 def _scale_fn(scale_mode):
@@ -104,6 +127,23 @@ def quantize_values(x, s):
     return e4m3_encode(y)
 
 
+def quantize_values_mul(x, m):
+    """q = E4M3(float32(x * m)), elementwise with broadcasting."""
+    x = np.asarray(x, dtype=np.float32)
+    m = np.asarray(m, dtype=np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        y = x * m  # float32 product, IEEE round to nearest
+    return e4m3_encode(y)
+
+
+def _group_codes(x, amax, s, scale_mode):
+    """Codes of the values x (broadcast against their group's amax and s)
+    under the mode's rule: x / s, or x * m in the reciprocal-multiply mode."""
+    if scale_mode == "mul_recip":
+        return quantize_values_mul(x, group_multiplier(amax))
+    return quantize_values(x, s)
+
+
 def quantize_act_1x128(x, scale_mode="amax448"):
     """Quantise X [R, C] in 1x128 groups along C.
 
@@ -114,7 +154,7 @@ def quantize_act_1x128(x, scale_mode="amax448"):
     xg = x.reshape(R, C // GROUP, GROUP)
     amax = np.nanmax(np.abs(xg), axis=2) if xg.size else np.zeros((R, C // GROUP), np.float32)
     s = _scale_fn(scale_mode)(amax)  # [R, C/128]
-    q = quantize_values(xg, s[:, :, None]).reshape(R, C)
+    q = _group_codes(xg, amax[:, :, None], s[:, :, None], scale_mode).reshape(R, C)
     return q, np.ascontiguousarray(s.T)
 
 
@@ -139,7 +179,7 @@ def quantize_w_128x128(w, scale_mode="amax448"):
     wb = w.reshape(N // GROUP, GROUP, K // GROUP, GROUP)
     amax = np.nanmax(np.abs(wb), axis=(1, 3)) if wb.size else np.zeros((N // GROUP, K // GROUP), np.float32)
     s = _scale_fn(scale_mode)(amax)  # [N/128, K/128]
-    q = quantize_values(wb, s[:, None, :, None]).reshape(N, K)
+    q = _group_codes(wb, amax[:, None, :, None], s[:, None, :, None], scale_mode).reshape(N, K)
     return q, np.ascontiguousarray(q.T), s
 
 

@@ -7,7 +7,11 @@ single-element perturbations, and the paper's qualitative claim that local
 scales beat one scale per tensor when outliers are present.  The power-of-two
 mode is pinned by its own worked group, an exact-rational search for the
 scale over every positive bf16 amax, and torch's float8 cast of the exactly
-scaled values.
+scaled values.  The reciprocal-multiply mode is pinned by its own worked
+group (where it and the division give different codes), an exact-rational
+evaluation of its rule with a hand-written float32 rounding, and closed-form
+properties: every bf16 amax codes to 448, and codes stay within one E4M3
+step of the division's.
 """
 
 import numpy as np
@@ -258,3 +262,121 @@ def test_pow2_weights_and_tokens_use_the_same_rule():
     assert np.array_equal(qt, q2) and np.array_equal(st, s2)
     with pytest.raises(ValueError):
         quant.quantize_act_1x128(x, scale_mode="ue8m0")
+
+
+# ------------------------------------------------------- reciprocal multiply
+
+
+def test_mul_recip_worked_example_group():
+    rows = read_golden("mul_recip_quant_worked_example.txt")
+    assert rows[0][0] == "scale" and rows[1][0] == "multiplier"
+    want_s, want_m = float.fromhex(rows[0][1]), float.fromhex(rows[1][1])
+    x = np.zeros((1, 128), np.float32)
+    want = np.zeros(128, np.uint8)
+    want_div = np.zeros(128, np.uint8)
+    for pos, xv, code, code_div in rows[2:]:
+        x[0, int(pos)] = np.float32(float(xv))
+        want[int(pos)] = int(code, 16)
+        want_div[int(pos)] = int(code_div, 16)
+    assert np.array_equal(bf16_exact(x).view(np.uint32), x.view(np.uint32))
+    assert float(quant.group_multiplier(np.float32(13.0))) == want_m
+    q, s = quant.quantize_act_1x128(np.tile(x, (128, 1)), scale_mode="mul_recip")
+    assert np.all(s == want_s)
+    assert np.array_equal(q[0], want) and np.array_equal(q[127], want)
+    qd, sd = quant.quantize_act_1x128(np.tile(x, (128, 1)))
+    assert np.array_equal(sd, s) and np.array_equal(qd[0], want_div)
+
+
+def _rn_f32(v):
+    """The float32 nearest to the Fraction v (ties to even, gradual underflow),
+    +-inf where it rounds beyond the largest finite float32."""
+    from fractions import Fraction
+    if v == 0:
+        return 0.0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 23)
+    n = a // quantum
+    r = a - n * quantum
+    if 2 * r > quantum or (2 * r == quantum and n % 2 == 1):
+        n += 1
+    out = n * quantum
+    mag = float("inf") if out >= Fraction(2) ** 128 else float(out)
+    return -mag if v < 0 else mag
+
+
+def test_mul_recip_codes_match_exact_rational_evaluation():
+    from fractions import Fraction
+    wl = workloads.make("mlp_down")
+    x = workloads.tensor(wl, "x").float().numpy()[:64, :256].copy()
+    # two groups with extreme amax: a tiny one whose multiplier saturates,
+    # and one near the top of the bf16 range
+    x[62, :128] *= np.float32(2.0 ** -126)
+    x[63, 128:] *= np.float32(2.0 ** 100)
+    x = bf16_exact(x)
+    x = np.concatenate([x, -x], axis=0)  # 128 rows
+    q, s = quant.quantize_act_1x128(x, scale_mode="mul_recip")
+    fmax = float(np.finfo(np.float32).max)
+    ys = np.zeros(x.shape, np.float32)
+    for r in range(x.shape[0]):
+        for g in range(2):
+            xs = x[r, 128 * g:128 * (g + 1)]
+            amax = Fraction(float(np.abs(xs).max()))
+            assert float(s[g, r]) == _rn_f32(amax / 448)
+            m = min(_rn_f32(Fraction(448) / amax), fmax)
+            if r % 64 == 62 and g == 0:
+                assert m == fmax  # the saturated multiplier is exercised
+            for c, xv in enumerate(xs):
+                # m > 0: the product has the sign of x, zeros included
+                ys[r, 128 * g + c] = np.copysign(_rn_f32(Fraction(float(xv)) * Fraction(m)), xv)
+    ref = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+def test_mul_recip_properties_over_every_bf16_amax():
+    from fractions import Fraction
+    bits = np.arange(1, 0x7F80, dtype=np.uint32) << 16  # every positive finite bf16 value
+    amax = bits.view(np.float32)
+    m = quant.group_multiplier(amax)
+    fmax = float(np.finfo(np.float32).max)
+    for a, mv in zip(amax[::11], m[::11]):
+        assert float(mv) == min(_rn_f32(Fraction(448) / Fraction(float(a))), fmax), a
+    # every group's amax codes to 448 unless its multiplier saturates
+    n = amax.size - amax.size % 128
+    x = amax[:n].reshape(-1, 128)  # rows of increasing bf16 values: amax is the last
+    x = x[: (x.shape[0] // 128) * 128]
+    q, s = quant.quantize_act_1x128(x, scale_mode="mul_recip")
+    top = q[:, 127]
+    unsat = quant.group_multiplier(x[:, 127]) < np.float32(fmax)
+    assert np.all(top[unsat] == 0x7E) and np.all(top[~unsat] < 0x7E)
+    # within one E4M3 step of the division, same sign, same scales
+    qd, sd = quant.quantize_act_1x128(x)
+    assert np.array_equal(s, sd)
+    diff = np.abs((q & 0x7F).astype(int) - (qd & 0x7F).astype(int))
+    assert np.all(diff[unsat] <= 1) and np.array_equal(q & 0x80, qd & 0x80)
+
+
+@pytest.mark.parametrize("name,tag", [("tiny", "x"), ("tiny", "w")])
+def test_mul_recip_invariants_rows_tokens_weights(name, tag):
+    wl = workloads.make(name)
+    x = workloads.tensor(wl, tag).float().numpy()
+    R, C = x.shape
+    q, s = quant.quantize_act_1x128(x, scale_mode="mul_recip")
+    assert _roundtrip_ok(x, q, np.repeat(s.T, 128, axis=1))
+    qd, sd = quant.quantize_act_1x128(x)
+    assert np.array_equal(s, sd)
+    assert np.all(np.abs((q & 0x7F).astype(int) - (qd & 0x7F).astype(int)) <= 1)
+    qT, sT = quant.quantize_act_tokens_1x128(x, scale_mode="mul_recip")
+    q2, s2 = quant.quantize_act_1x128(np.ascontiguousarray(x.T), scale_mode="mul_recip")
+    assert np.array_equal(qT, q2) and np.array_equal(sT, s2)
+    wq, wqT, ws = quant.quantize_w_128x128(x, scale_mode="mul_recip")
+    assert np.array_equal(wqT, wq.T)
+    assert _roundtrip_ok(x, wq, np.repeat(np.repeat(ws, 128, axis=0), 128, axis=1))
+    blk = np.abs(x.reshape(R // 128, 128, C // 128, 128)).max(axis=(1, 3))
+    mb = quant.group_multiplier(blk)
+    ref = quant.quantize_values_mul(x.reshape(R // 128, 128, C // 128, 128), mb[:, None, :, None]).reshape(R, C)
+    assert np.array_equal(wq, ref)
