@@ -68,24 +68,23 @@ bfp8_status device_state(DeviceState** out) {
     }
     cudaError_t e = cudaSuccess;
     // two quantiser CTAs per SM need the largest shared-memory carveout
-#define BFP8_SET_QUANT_SMEM(W, MODE, POW2)                                                                     \
-  if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, POW2>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             kQuantSmemBytes);                                                                  \
-  if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, POW2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    BFP8_SET_QUANT_SMEM(false, kQRows, false)
-    BFP8_SET_QUANT_SMEM(false, kQCols, false)
-    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, false)
-    BFP8_SET_QUANT_SMEM(true, kQRows, false)
-    BFP8_SET_QUANT_SMEM(true, kQCols, false)
-    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, false)
-    BFP8_SET_QUANT_SMEM(false, kQRows, true)
-    BFP8_SET_QUANT_SMEM(false, kQCols, true)
-    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, true)
-    BFP8_SET_QUANT_SMEM(true, kQRows, true)
-    BFP8_SET_QUANT_SMEM(true, kQCols, true)
-    BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, true)
+#define BFP8_SET_QUANT_SMEM(W, MODE, SCALE)                                                                     \
+  if (e == cudaSuccess)                                                                                          \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             kQuantSmemBytes);                                                                   \
+  if (e == cudaSuccess)                                                                                          \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+#define BFP8_SET_QUANT_SMEM_ALL(SCALE)                  \
+  BFP8_SET_QUANT_SMEM(false, kQRows, SCALE)             \
+  BFP8_SET_QUANT_SMEM(false, kQCols, SCALE)             \
+  BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, SCALE)    \
+  BFP8_SET_QUANT_SMEM(true, kQRows, SCALE)              \
+  BFP8_SET_QUANT_SMEM(true, kQCols, SCALE)              \
+  BFP8_SET_QUANT_SMEM(true, kQRows | kQCols, SCALE)
+    BFP8_SET_QUANT_SMEM_ALL(kScaleAmax448)
+    BFP8_SET_QUANT_SMEM_ALL(kScalePow2)
+    BFP8_SET_QUANT_SMEM_ALL(kScaleMulRecip)
+#undef BFP8_SET_QUANT_SMEM_ALL
 #undef BFP8_SET_QUANT_SMEM
 #define BFP8_SET_GEMM_SMEM(BN, MODE, EPI)                                                                     \
   if (e == cudaSuccess)                                                                                        \
@@ -375,19 +374,27 @@ bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap&
 // Persistent quantiser grid: two CTAs per SM (each streams its tiles
 // through a 3-deep shared-memory ring).  The tile walk and the TMA
 // coordinates are 32-bit: C up to 2^27 and fewer than 2^31 tiles.
-template <bool kWeight, bool kPow2>
+template <bool kWeight, int kScale>
 bfp8_status launch_quant_mode(const CUtensorMap& tm, const QuantParams& p, unsigned grid, cudaStream_t st) {
   const int mode = (p.q ? kQRows : 0) | (p.qT ? kQCols : 0);
   if (mode == kQRows)
-    quantize_tile_kernel<kWeight, kQRows, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   else if (mode == kQCols)
-    quantize_tile_kernel<kWeight, kQCols, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   else
-    quantize_tile_kernel<kWeight, kQRows | kQCols, kPow2><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows | kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
   return BFP8_OK;
 }
 
-bfp8_status launch_quant(QuantParams p, bool weight, bool pow2, cudaStream_t st) {
+template <bool kWeight>
+bfp8_status launch_quant_scale(const CUtensorMap& tm, const QuantParams& p, unsigned grid, int scale_mode,
+                               cudaStream_t st) {
+  if (scale_mode == kScalePow2) return launch_quant_mode<kWeight, kScalePow2>(tm, p, grid, st);
+  if (scale_mode == kScaleMulRecip) return launch_quant_mode<kWeight, kScaleMulRecip>(tm, p, grid, st);
+  return launch_quant_mode<kWeight, kScaleAmax448>(tm, p, grid, st);
+}
+
+bfp8_status launch_quant(QuantParams p, bool weight, int scale_mode, cudaStream_t st) {
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
@@ -399,10 +406,8 @@ bfp8_status launch_quant(QuantParams p, bool weight, bool pow2, cudaStream_t st)
   CUtensorMap tm;
   if ((s = make_quant_tmap(&tm, p.x, p.R, p.C)) != BFP8_OK) return s;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
-  if (weight)
-    s = pow2 ? launch_quant_mode<true, true>(tm, p, grid, st) : launch_quant_mode<true, false>(tm, p, grid, st);
-  else
-    s = pow2 ? launch_quant_mode<false, true>(tm, p, grid, st) : launch_quant_mode<false, false>(tm, p, grid, st);
+  s = weight ? launch_quant_scale<true>(tm, p, grid, scale_mode, st)
+             : launch_quant_scale<false>(tm, p, grid, scale_mode, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -468,7 +473,7 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   if (g.splits == 1) {
     if (Cq == nullptr || fused_here) return BFP8_OK;  // (Cacc: added by the epilogue)
     QuantParams qp{static_cast<const uint16_t*>(C), M, N, Cq, sCq, nullptr, nullptr, dev->wait_ns, 0u, 0u};
-    return launch_quant(qp, false, false, stream);
+    return launch_quant(qp, false, kScaleAmax448, stream);
   }
   const int64_t groups = M * (N / 128);
   const int rgrid = static_cast<int>(std::min<int64_t>((groups + 7) / 8, int64_t(dev->sms) * 16));
@@ -478,7 +483,12 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   return cuda_status(cudaGetLastError());
 }
 
-bool scale_mode_ok(int mode) { return mode == BFP8_SCALE_AMAX448 || mode == BFP8_SCALE_POW2; }
+static_assert(kScaleAmax448 == BFP8_SCALE_AMAX448 && kScalePow2 == BFP8_SCALE_POW2 &&
+                  kScaleMulRecip == BFP8_SCALE_MUL_RECIP,
+              "kernel scale modes are numbered as the ABI's");
+bool scale_mode_ok(int mode) {
+  return mode == BFP8_SCALE_AMAX448 || mode == BFP8_SCALE_POW2 || mode == BFP8_SCALE_MUL_RECIP;
+}
 
 bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
                            int scale_mode, cudaStream_t stream) {
@@ -492,7 +502,7 @@ bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, floa
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
   QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns, 0u, 0u};
-  return launch_quant(p, false, scale_mode == BFP8_SCALE_POW2, stream);
+  return launch_quant(p, false, scale_mode, stream);
 }
 
 bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s, int scale_mode,
@@ -505,7 +515,7 @@ bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_
   bfp8_status st = device_state(&dev);
   if (st != BFP8_OK) return st;
   QuantParams p{static_cast<const uint16_t*>(w), N, K, q, s, qT, nullptr, dev->wait_ns, 0u, 0u};
-  return launch_quant(p, true, scale_mode == BFP8_SCALE_POW2, stream);
+  return launch_quant(p, true, scale_mode, stream);
 }
 
 // Workspace carving for the fused linear calls: consecutive 256-byte aligned

@@ -265,16 +265,39 @@ __device__ __forceinline__ GroupScale make_group_scale_pow2(float amax) {
   return g;
 }
 
-// Whether a group scale of the given mode is on the fast (multiply or FMA)
-// path; restates GroupScale::exact from s alone.
-template <bool kPow2>
-__device__ __forceinline__ bool scale_fast(float s) {
-  return kPow2 ? s >= 0x1p-127f : (s >= 0x1p-80f && s <= 0x1p+100f);
+// Reciprocal-multiply mode: the stored scale is amax/448 as above, and the
+// codes are E4M3(fp32_rn(x * m)) with one multiplier per group,
+// m = fp32_rn(448 / amax) (one IEEE division per group), saturated at the
+// largest finite fp32 (reached only for amax below about 2^-119); 1 for an
+// all-zero group.  GroupScale::r carries m; every group is on the multiply
+// path.
+__device__ __forceinline__ GroupScale make_group_scale_recip(float amax) {
+  GroupScale g;
+  g.s = group_scale(amax);
+  g.r = amax == 0.0f ? 1.0f : fminf(__fdiv_rn(448.0f, amax), 0x1.FFFFFEp+127f);
+  g.exact = true;
+  return g;
 }
 
-template <bool kPow2>
+// Scale modes, numbered as the C ABI's bfp8_scale_mode.
+constexpr int kScaleAmax448 = 0;
+constexpr int kScalePow2 = 1;
+constexpr int kScaleMulRecip = 2;
+
+// Whether a group scale of the given mode is on the fast (multiply or FMA)
+// path; restates GroupScale::exact from s alone.
+template <int kScale>
+__device__ __forceinline__ bool scale_fast(float s) {
+  if constexpr (kScale == kScalePow2) return s >= 0x1p-127f;
+  if constexpr (kScale == kScaleMulRecip) return true;
+  return s >= 0x1p-80f && s <= 0x1p+100f;
+}
+
+template <int kScale>
 __device__ __forceinline__ GroupScale make_scale(float amax) {
-  return kPow2 ? make_group_scale_pow2(amax) : make_group_scale(amax);
+  if constexpr (kScale == kScalePow2) return make_group_scale_pow2(amax);
+  if constexpr (kScale == kScaleMulRecip) return make_group_scale_recip(amax);
+  return make_group_scale(amax);
 }
 
 // |v| with the sign of x.
@@ -315,10 +338,11 @@ __device__ __forceinline__ uint32_t quant4_exact(uint32_t w0, uint32_t w1, float
   return e4m3x4(q0.x, q0.y, q1.x, q1.y) | signs;
 }
 
-// Codes of the four bf16 values of words w0, w1 under a power-of-two scale
-// (r2 = 2^-k in both halves): exact products, then the casts.  The product
-// keeps the sign of a zero, so no sign restore is needed.
-__device__ __forceinline__ uint32_t quant4_pow2(uint32_t w0, uint32_t w1, float2 r2) {
+// Codes of the four bf16 values of words w0, w1 from their products with a
+// positive group multiplier (r2 = m in both halves): E4M3(fp32_rn(x * m)).
+// Under a power-of-two scale (m = 2^-k) the product is exact.  It keeps the
+// sign of a zero, so no sign restore is needed.
+__device__ __forceinline__ uint32_t quant4_mul(uint32_t w0, uint32_t w1, float2 r2) {
   const float2 a = fmul2(make_float2(bf16lo(w0), bf16hi(w0)), r2);
   const float2 b = fmul2(make_float2(bf16lo(w1), bf16hi(w1)), r2);
   return e4m3x4(a.x, a.y, b.x, b.y);

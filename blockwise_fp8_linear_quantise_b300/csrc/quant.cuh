@@ -8,7 +8,10 @@
 // Per group: amax = max|x| (NaN ignored); s = amax/448 in IEEE fp32 (1 when
 // amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  The quotient is formed
 // exactly by FMA correction steps (GroupScale), so codes and scales match a
-// plain CPU evaluation bit for bit.
+// plain CPU evaluation bit for bit.  Two other scale modes share the kernel:
+// power-of-two scales (s = the smallest 2^k >= amax/448, codes from the exact
+// product x * 2^-k) and the reciprocal multiply (s = amax/448 stored, codes
+// E4M3(fp32_rn(x * fp32_rn(448/amax)))): both form each code from one product.
 //
 // Work decomposition.  The input is cut into 128x128 bf16 tiles (32 KB),
 // walked in row-major order by a persistent grid (two CTAs per SM).  A CTA
@@ -95,13 +98,13 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
 // 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i),
 // one group.  Groups with extreme scales (g.exact false) take the IEEE
 // division.
-template <bool kPow2>
+template <int kScale>
 __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
   if (g.exact) {
     const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-    if constexpr (kPow2)
-      return make_uint4(quant4_pow2(w[0], w[1], r2), quant4_pow2(w[2], w[3], r2), quant4_pow2(w[4], w[5], r2),
-                        quant4_pow2(w[6], w[7], r2));
+    if constexpr (kScale != kScaleAmax448)
+      return make_uint4(quant4_mul(w[0], w[1], r2), quant4_mul(w[2], w[3], r2), quant4_mul(w[4], w[5], r2),
+                        quant4_mul(w[6], w[7], r2));
     else
       return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
                         quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
@@ -113,22 +116,22 @@ __device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupSca
 }
 
 // The same on the fast path only (every group of the tile has g.exact).
-template <bool kPow2>
+template <int kScale>
 __device__ __forceinline__ uint4 quant16w_fast(const uint32_t (&w)[8], const GroupScale& g) {
   const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-  if constexpr (kPow2)
-    return make_uint4(quant4_pow2(w[0], w[1], r2), quant4_pow2(w[2], w[3], r2), quant4_pow2(w[4], w[5], r2),
-                      quant4_pow2(w[6], w[7], r2));
+  if constexpr (kScale != kScaleAmax448)
+    return make_uint4(quant4_mul(w[0], w[1], r2), quant4_mul(w[2], w[3], r2), quant4_mul(w[4], w[5], r2),
+                      quant4_mul(w[6], w[7], r2));
   else
     return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
                       quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
 }
 
 // 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
-template <bool kFast, bool kPow2>
+template <bool kFast, int kScale>
 __device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  return kFast ? quant16w_fast<kPow2>(w, g) : quant16w<kPow2>(w, g);
+  return kFast ? quant16w_fast<kScale>(w, g) : quant16w<kScale>(w, g);
 }
 
 // Values k and k+1 of one column (element kHalf of word kWord of row slices
@@ -140,12 +143,12 @@ __device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
 }
 
 // 16 codes of one column over 16 rows, one group.  Codes in row order.
-template <int kWord, int kHalf, bool kFast, bool kPow2>
+template <int kWord, int kHalf, bool kFast, int kScale>
 __device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupScale& g) {
   uint32_t w[8];
 #pragma unroll
   for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
-  return kFast ? quant16w_fast<kPow2>(w, g) : quant16w<kPow2>(w, g);
+  return kFast ? quant16w_fast<kScale>(w, g) : quant16w<kScale>(w, g);
 }
 
 // Warp 0 fetches tile (rt, ct) into ring slot `buf` with 32 TMA boxes (one
@@ -162,30 +165,30 @@ __device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t C, u
 // Codes of this warp's row and column slices of one tile, stored to global
 // memory.  kFast: every group scale of the warp is on the FMA path, so the
 // whole body is one branch-free block the compiler can interleave.
-template <int kMode, bool kFast, bool kPow2>
+template <int kMode, bool kFast, int kScale>
 __device__ __forceinline__ void quant_tile_codes(const uint4 (&rv)[8], const uint2 (&cv)[16], const GroupScale& grow,
                                                  const GroupScale (&gc)[4], uint8_t* qrow, uint8_t* qcol,
                                                  int64_t R) {
   if constexpr ((kMode & kQRows) != 0) {
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast, kPow2>(rv[2 * m], rv[2 * m + 1], grow);
+      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast, kScale>(rv[2 * m], rv[2 * m + 1], grow);
   }
   if constexpr ((kMode & kQCols) != 0) {
     GroupScale g[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_fast<kPow2>(gc[k].s)};
-    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast, kPow2>(cv, g[0]);
-    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast, kPow2>(cv, g[1]);
-    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast, kPow2>(cv, g[2]);
-    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast, kPow2>(cv, g[3]);
+    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_fast<kScale>(gc[k].s)};
+    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast, kScale>(cv, g[0]);
+    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast, kScale>(cv, g[1]);
+    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast, kScale>(cv, g[2]);
+    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast, kScale>(cv, g[3]);
   }
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
 // kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
-// kPow2: power-of-two scales (make_group_scale_pow2) instead of amax/448.
-template <bool kWeight, int kMode, bool kPow2>
+// kScale: the scale mode (kScaleAmax448, kScalePow2 or kScaleMulRecip).
+template <bool kWeight, int kMode, int kScale>
 __global__ void __launch_bounds__(kQuantThreads, 2)
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       float bm = rbuf[0];
 #pragma unroll
       for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
-      grow = make_scale<kPow2>(bm);
+      grow = make_scale<kScale>(bm);
 #pragma unroll
       for (int k = 0; k < 4; ++k) gc[k] = grow;
       all_exact = grow.exact;  // uniform over the block
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     } else {
       bool ok = true;
       if constexpr (kRows) {
-        grow = make_scale<kPow2>(row_m);
+        grow = make_scale<kScale>(row_m);
         ok = grow.exact;
         if (hh == 0) p.s[static_cast<int64_t>(cur.ct) * p.R + r0 + wrow] = grow.s;
       }
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
         // hold those of this lane's columns
         const int sel = g & 3;
         const uint32_t mw = sel < 2 ? m01 : m23;
-        const GroupScale gcol = make_scale<kPow2>(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
+        const GroupScale gcol = make_scale<kScale>(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
         ok = ok && gcol.exact;
         if (g < 4) p.sT[static_cast<int64_t>(cur.rt) * p.C + c0 + 16 * warp + 4 * cq + g] = gcol.s;
 #pragma unroll
@@ -347,10 +350,10 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     // codes
     uint8_t* qrow = kRows ? p.q + (r0 + wrow) * p.C + c0 + 16 * hh : nullptr;
     uint8_t* qcol = kCols ? p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg : nullptr;
-    if (all_exact)
-      quant_tile_codes<kMode, true, kPow2>(rv, cv, grow, gc, qrow, qcol, p.R);
+    if (kScale == kScaleMulRecip || all_exact)  // the multiplier mode has no slow path
+      quant_tile_codes<kMode, true, kScale>(rv, cv, grow, gc, qrow, qcol, p.R);
     else
-      quant_tile_codes<kMode, false, kPow2>(rv, cv, grow, gc, qrow, qcol, p.R);
+      quant_tile_codes<kMode, false, kScale>(rv, cv, grow, gc, qrow, qcol, p.R);
   }
   // Leave no copy in flight into this CTA's shared memory: after an early
   // exit at local tile j, warp 0 (which issues every copy) waits (bounded)

@@ -55,7 +55,7 @@ def _out(t, dtype, shape, device, name):
     return _need(t, dtype, shape, name)
 
 
-SCALE_MODES = {"amax448": 0, "pow2": 1}
+SCALE_MODES = {"amax448": 0, "pow2": 1, "mul_recip": 2}
 
 
 def _scale_mode(scale_mode):
@@ -71,7 +71,8 @@ def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=N
 
     rows   -> q [M, K] uint8 (groups along K), s [K/128, M] float32
     tokens -> qT [K, M] uint8 (groups of 128 tokens per column), sT [M/128, K]
-    scale_mode "amax448" (s = amax/448) or "pow2" (smallest power of two >= amax/448).
+    scale_mode "amax448" (s = amax/448, codes of x/s), "pow2" (smallest power of two >= amax/448) or
+    "mul_recip" (s = amax/448, codes of x * fp32(448/amax)).
     Returns (q, s, qT, sT) with None for outputs not requested.
     """
     M, K = x.shape

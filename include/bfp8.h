@@ -65,8 +65,9 @@ typedef enum {
 
 /* How a group's scale s is chosen from its amax (the largest |x|). */
 typedef enum {
-  BFP8_SCALE_AMAX448 = 0, /* s = fp32(amax / 448): the default, used by every entry point without _ex */
-  BFP8_SCALE_POW2 = 1     /* s = smallest power of two >= amax / 448 (the paper's SM120 power-of-two scales) */
+  BFP8_SCALE_AMAX448 = 0,   /* s = fp32(amax / 448): the default, used by every entry point without _ex */
+  BFP8_SCALE_POW2 = 1,      /* s = smallest power of two >= amax / 448 (the paper's SM120 power-of-two scales) */
+  BFP8_SCALE_MUL_RECIP = 2  /* s = fp32(amax / 448); codes from x * fp32(448 / amax) instead of x / s */
 } bfp8_scale_mode;
 
 /*
@@ -113,10 +114,19 @@ bfp8_status bfp8_quantize_w_128x128(const void* w, int64_t N, int64_t K,
  *   BFP8_SCALE_POW2     s = 2^k, the smallest power of two with s >= amax/448
  *                       (so nothing saturates and the group's largest |x|/s
  *                       lies in (224, 448]); 1 for an all-zero group.
- * In both modes q = E4M3_rn_satfinite(fp32(x / s)); with a power-of-two s the
- * division is an exact scaling.  The scales are fp32 in both modes, so the
- * GEMM and linear entry points consume either.  An unknown scale_mode returns
- * BFP8_EINVAL.
+ *   BFP8_SCALE_MUL_RECIP  s = fp32(amax / 448) as in the default mode, but the
+ *                       codes multiply by the group's reciprocal instead of
+ *                       dividing by s (the pages do not fix which; this is the
+ *                       other reading): q = E4M3_rn_satfinite(fp32(x * m)),
+ *                       m = fp32(448 / amax), saturated at the largest finite
+ *                       fp32 (amax below about 2^-119); m = 1 for an all-zero
+ *                       group.  One division per group instead of per value;
+ *                       a few codes near E4M3 rounding midpoints differ from
+ *                       the default mode's by one step.
+ * In the first two modes q = E4M3_rn_satfinite(fp32(x / s)); with a
+ * power-of-two s the division is an exact scaling.  The scales are fp32 in
+ * every mode, so the GEMM and linear entry points consume any of them.  An
+ * unknown scale_mode returns BFP8_EINVAL.
  */
 bfp8_status bfp8_quantize_act_1x128_ex(const void* x, int64_t M, int64_t K,
                                        uint8_t* q, float* s, uint8_t* qT, float* sT,
@@ -267,8 +277,9 @@ bfp8_status bfp8_linear_fwd_prequantised(const void* X, const uint8_t* Wq, const
 /*
  * bfp8_linear_fwd / bfp8_linear_bwd with an explicit scale rule for every
  * quantisation they run (see bfp8_quantize_act_1x128_ex).  The saved tensors
- * carry fp32 scales in either mode; bfp8_linear_bwd_ex takes the mode for
- * the output-gradient quantisation only.  Arguments, workspaces and errors
+ * carry fp32 scales in every mode; bfp8_linear_bwd_ex takes the mode for
+ * the output-gradient quantisation only (the mode need not match the
+ * forward's).  Arguments, workspaces and errors
  * are otherwise those of the calls without _ex; an unknown scale_mode
  * returns BFP8_EINVAL.
  */

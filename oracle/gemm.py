@@ -124,29 +124,30 @@ def accumulate_into(main, acc):
     return (np.asarray(main, dtype=np.float32) + np.asarray(acc, dtype=np.float32)).astype(np.float32)
 
 
-def linear_fwd(X, W):
+def linear_fwd(X, W, scale_mode="amax448"):
     """Quantise W (128x128) and X (1x128 along features, and along tokens for
-    the later wgrad), then run fprop.
+    the later wgrad) under the quantisers' scale_mode, then run fprop.
 
     Returns (Y bf16-valued float32 [M, N], saved dict).  ``saved`` holds what
     the backward pass reuses: FP8 is the storage format of the saved
     activation (section 3.2), and W is re-quantised on every use.
     """
-    Wq, WqT, sW = quant.quantize_w_128x128(W)
-    Xq, sX = quant.quantize_act_1x128(X)
-    XqT, sXT = quant.quantize_act_tokens_1x128(X)
+    Wq, WqT, sW = quant.quantize_w_128x128(W, scale_mode)
+    Xq, sX = quant.quantize_act_1x128(X, scale_mode)
+    XqT, sXT = quant.quantize_act_tokens_1x128(X, scale_mode)
     _, Y = fprop(Xq, sX, Wq, sW)
     saved = dict(Wq=Wq, WqT=WqT, sW=sW, Xq=Xq, sX=sX, XqT=XqT, sXT=sXT)
     return Y, saved
 
 
-def linear_bwd(dY, saved, main_grad=None):
-    """Quantise dY along features (for dgrad) and along tokens (for wgrad),
-    then run dgrad and wgrad.  Returns (dX, dW) as bf16-valued float32; with
-    main_grad (fp32 [N, K]) dW is instead main_grad + the wgrad accumulator
-    (accumulate_into), returned as a new float32 array."""
-    dYq, sdY = quant.quantize_act_1x128(dY)
-    dYqT, sdYT = quant.quantize_act_tokens_1x128(dY)
+def linear_bwd(dY, saved, main_grad=None, scale_mode="amax448"):
+    """Quantise dY along features (for dgrad) and along tokens (for wgrad)
+    under scale_mode, then run dgrad and wgrad.  Returns (dX, dW) as
+    bf16-valued float32; with main_grad (fp32 [N, K]) dW is instead
+    main_grad + the wgrad accumulator (accumulate_into), returned as a new
+    float32 array."""
+    dYq, sdY = quant.quantize_act_1x128(dY, scale_mode)
+    dYqT, sdYT = quant.quantize_act_tokens_1x128(dY, scale_mode)
     _, dX = dgrad(dYq, sdY, saved["WqT"], saved["sW"])
     acc, dW = wgrad(dYqT, sdYT, saved["XqT"], saved["sXT"])
     if main_grad is not None:

@@ -32,7 +32,7 @@ def _eager(X, W, dY, scale_mode):
     return dict(Y=Y, dX=dX, dW=dW, q=q, s=s, qT=qT, sT=sT, **{"saved_" + k: v for k, v in saved.items()})
 
 
-@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_linear_step_replays_from_a_cuda_graph(scale_mode):
     M, N, K = 512, 640, 384
     X, W, dY = _inputs(1)

@@ -52,7 +52,7 @@ def test_linear_repeat_is_deterministic():
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_prequantised_weights_give_the_same_forward(scale_mode):
     """Weights quantised once (cached across micro-steps) and passed to the
     prequantised forward give linear_fwd's output and saved tensors bit for

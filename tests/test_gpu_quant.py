@@ -1,5 +1,5 @@
 """GPU quantisers vs the CPU oracle: E4M3 codes and fp32 scales bit-exact, in
-both scale modes (amax/448 and the power-of-two mode)."""
+every scale mode (amax/448, power-of-two, and the reciprocal multiply)."""
 
 import numpy as np
 import pytest
@@ -56,7 +56,7 @@ def test_multi_tile_shapes(M, K):
     check_w(x)
 
 
-@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_edge_values(scale_mode):
     # zeros (scale 1), signed zeros, subnormal-scale groups, huge groups, ties
     M, K = 256, 384
@@ -78,7 +78,7 @@ def test_edge_values(scale_mode):
     check_w(xb, scale_mode)
 
 
-@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_every_bf16_bit_pattern(scale_mode):
     bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
     fin = bits[np.isfinite(bits)]
@@ -114,7 +114,7 @@ def test_every_bf16_value_below_a_fixed_amax(amax):
     check_w(xb)
 
 
-@pytest.mark.parametrize("scale_mode", ["amax448", "pow2"])
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_every_bf16_value_as_group_amax(scale_mode):
     """Row group g (128 values along K) has amax = the g-th positive finite
     bf16 value, so every scale amax/448 reachable from bf16 inputs is formed
@@ -206,11 +206,84 @@ def test_pow2_linear_layer_against_oracle():
     assert rel_fro(np32(Y), want) <= REL_FRO_TOL
 
 
+# ------------------------------------------------------- reciprocal multiply
+
+
+def _below_amax_groups(amax):
+    """Groups of 256 columns: +-amax, then every finite bf16 value of smaller
+    magnitude (127 per 128-group), zero-padded to whole tiles."""
+    a = np.float32(workloads.to_bf16(np.array([amax], np.float32)).float().numpy()[0])
+    bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    vals = bits[np.isfinite(bits) & (np.abs(bits) <= a)]
+    per = 127
+    groups = -(-vals.size // per)
+    groups += (-groups) % 2
+    padded = np.zeros(groups * per, np.float32)
+    padded[: vals.size] = vals
+    g = padded.reshape(groups, per)
+    first = np.where(np.arange(groups) % 2 == 0, a, -a).astype(np.float32)[:, None]
+    x = np.concatenate([first, g], axis=1).reshape(-1, 256)
+    rows = -(-x.shape[0] // 128) * 128
+    full = np.zeros((rows, 256), np.float32)
+    full[: x.shape[0]] = x
+    return workloads.to_bf16(full)
+
+
+@pytest.mark.parametrize("amax", [13.0, 3.0, 0.7109375, 123.5, 1.0e-30, 5.0e-39, 2.5e38, 1.0])
+def test_mul_recip_every_bf16_value_below_a_fixed_amax(amax):
+    """The sweep of the amax/448 mode with codes from x * fp32(448/amax): the
+    products land on and around E4M3 midpoints (amax 13 puts x = 39 * 2^-16
+    exactly on one before rounding), and amax 5e-39 saturates the
+    multiplier at the largest finite fp32."""
+    xb = _below_amax_groups(amax)
+    check_act(xb, "mul_recip")
+    check_w(xb, "mul_recip")
+
+
+@pytest.mark.parametrize("name,tag", [("mlp_gateup", "x"), ("mlp_down", "dy"), ("attn_proj", "w_qkv")])
+def test_mul_recip_full_size_configs(name, tag):
+    t = bf16_input(name, tag)
+    if tag.startswith("w"):
+        check_w(t, "mul_recip")
+    else:
+        check_act(t, "mul_recip")
+
+
+def test_mul_recip_linear_layer_against_oracle():
+    """The reciprocal-multiply mode through the fused linear entry points:
+    saved FP8 tensors and scales bit-exact against the oracle's composed
+    linear in the same mode, outputs within the GEMM tolerance."""
+    from gpu_helpers import REL_FRO_TOL, rel_fro
+    from oracle import gemm as ogemm
+    rng = np.random.default_rng(41)
+    X = workloads.to_bf16(rng.standard_normal((384, 640)).astype(np.float32))
+    W = workloads.to_bf16((rng.standard_normal((512, 640)) * 0.02).astype(np.float32))
+    dY = workloads.to_bf16((rng.standard_normal((384, 512)) * 1e-3).astype(np.float32))
+    Y, saved = ops.linear_fwd(X.to(dev()), W.to(dev()), scale_mode="mul_recip")
+    dX, dW = ops.linear_bwd(dY.to(dev()), saved, scale_mode="mul_recip")
+    assert ops.sync_status() == 0
+    oY, osaved = ogemm.linear_fwd(np32(X), np32(W), scale_mode="mul_recip")
+    for k in ("WqT", "XqT"):
+        assert_codes_equal(u8(saved[k]), osaved[k], k)
+    for k in ("sW", "sXT"):
+        assert_scales_equal(saved[k].cpu().numpy(), osaved[k], k)
+    assert rel_fro(np32(Y), oY) <= REL_FRO_TOL
+    odX, odW = ogemm.linear_bwd(np32(dY), osaved, scale_mode="mul_recip")
+    assert rel_fro(np32(dX), odX) <= REL_FRO_TOL
+    assert rel_fro(np32(dW), odW) <= REL_FRO_TOL
+    # the same layer in the default mode differs only in a few codes
+    _, saved_d = ops.linear_fwd(X.to(dev()), W.to(dev()))
+    assert torch.equal(saved_d["sXT"], saved["sXT"]) and torch.equal(saved_d["sW"], saved["sW"])
+    step = (u8(saved_d["XqT"]) & 0x7F).astype(int) - (u8(saved["XqT"]) & 0x7F).astype(int)
+    assert np.abs(step).max() <= 1
+
+
 def test_unknown_scale_mode_is_rejected():
     from blockwise_fp8_linear_quantise_b300 import _lib
     x = torch.zeros((128, 128), dtype=torch.bfloat16, device=dev())
     q = torch.empty((128, 128), dtype=torch.uint8, device=dev())
     s = torch.empty((1, 128), dtype=torch.float32, device=dev())
     st = torch.cuda.current_stream().cuda_stream
-    assert _lib.load().bfp8_quantize_act_1x128_ex(x.data_ptr(), 128, 128, q.data_ptr(), s.data_ptr(), None, None,
-                                                  7, st) == 1
+    for bad in (3, 7, -1):
+        assert _lib.load().bfp8_quantize_act_1x128_ex(x.data_ptr(), 128, 128, q.data_ptr(), s.data_ptr(), None,
+                                                      None, bad, st) == 1
