@@ -198,23 +198,26 @@ __device__ __forceinline__ float group_scale(float amax) {
 
 // Per-group quantisation state.  A code is E4M3_rn_satfinite(fp32_rn(x / s)).
 // A division per element would dominate the quantisers' instruction count,
-// so the correctly rounded quotient Q = fp32_rn(x / s) is formed with
-// Markstein's FMA correction (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev., 1990;
-// as stated in Muller et al., Handbook of Floating-Point Arithmetic):
-//   r = RN(1/s)                      once per group (IEEE reciprocal);
-//   y = RN(x r)                      within 1.5 ulp of x/s;
-//   y = RN(y + r RN(x - s y))        one refinement: now within one ulp;
-//   Q = RN(y + r (x - s y))          x - s y is exact (FMA remainder of a
-//                                    faithful quotient), and with r = RN(1/s)
-//                                    the theorem gives Q = RN(x/s) (up to
-//                                    the sign of a zero, restored from x).
-// No step overflows or loses the remainder to underflow while s lies in
-// [2^-80, 2^100]: every quotient that can reach an E4M3 code (|x/s| >=
-// 2^-11) then has a remainder at or above 2^-137, and smaller quotients keep
-// the sign of x and stay far below the smallest E4M3 rounding boundary
-// (2^-10), so they still map to the right signed zero.  A group whose scale
-// lies outside that range (or is not finite) takes the IEEE division.
+// so the correctly rounded quotient Q = fp32_rn(x / s) is formed from the
+// group's reciprocal with one FMA correction (Markstein's step: P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev., 1990; as stated in Muller et al., Handbook of
+// Floating-Point Arithmetic):
+//   r  = RN(1/s)                     once per group (IEEE reciprocal);
+//   y0 = RN(x r)                     within 1.5 ulp of x/s;
+//   Q  = RN(y0 + r RN(x - s y0)).
+// For arbitrary x and s the theorem needs a faithful y (one more refinement
+// before the last step).  The inputs here are narrower: x is bf16, and s is
+// RN(amax/448) for a bf16 amax >= |x|.  Scaling x and amax by one power of two
+// leaves y0 and Q unchanged while s stays in [2^-80, 2^100] (r is then
+// normal, and a remainder that rounds is a normal fp32: it has more than 24
+// bits above its quantum ulp(s) ulp(y0) >= 2^-137), so one binade of amax
+// with every bf16 x covers all cases; evaluated exactly there (all 128
+// mantissas, every x in (0, amax]), Q equals fp32_rn(x / s) every time, and y0
+// alone misses some codes.  Quotients below 2^-11 (codes +-0) stay below the
+// smallest E4M3 rounding boundary (2^-10) whatever the remainder's rounding.
+// The sign of a zero quotient is restored from x.  A group whose scale lies
+// outside [2^-80, 2^100] (or is not finite) takes the IEEE division.
 struct GroupScale {
   float s;     // dequantisation scale amax/448 (1 for an all-zero group)
   float r;     // RN(1/s)
@@ -305,13 +308,13 @@ __device__ __forceinline__ float with_sign_of(float v, float x) {
   return __uint_as_float((__float_as_uint(v) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
 }
 
-// RN(x / s) for a pair, by the correction steps above (r2 = RN(1/s),
-// ns2 = -s, for each component), except that the sign of a zero result may
-// be lost (the sums of the correction steps turn -0 into +0).
+// RN(x / s) for a pair of bf16 values x of a group with s = RN(amax/448), by
+// the correction step above (r2 = RN(1/s), ns2 = -s, for each component),
+// except that the sign of a zero result may be lost (the correction's sum
+// turns -0 into +0).
 __device__ __forceinline__ float2 quotient_pair_unsigned_zero(float2 x, float2 r2, float2 ns2) {
-  float2 y = fmul2(x, r2);
-  y = ffma2(ffma2(y, ns2, x), r2, y);
-  return ffma2(ffma2(y, ns2, x), r2, y);
+  const float2 y0 = fmul2(x, r2);
+  return ffma2(ffma2(y0, ns2, x), r2, y0);
 }
 
 // Four E4M3 codes (byte i from q_i) in one register: two paired casts and

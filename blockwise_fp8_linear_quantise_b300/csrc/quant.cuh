@@ -7,7 +7,7 @@
 // 128x128 block for weights, each computed online from its own values.
 // Per group: amax = max|x| (NaN ignored); s = amax/448 in IEEE fp32 (1 when
 // amax == 0); q = E4M3_rn_satfinite(fp32_rn(x / s)).  The quotient is formed
-// exactly by FMA correction steps (GroupScale), so codes and scales match a
+// exactly by an FMA correction step (GroupScale), so codes and scales match a
 // plain CPU evaluation bit for bit.  Two other scale modes share the kernel:
 // power-of-two scales (s = the smallest 2^k >= amax/448, codes from the exact
 // product x * 2^-k) and the reciprocal multiply (s = amax/448 stored, codes

@@ -140,6 +140,10 @@ def test_fused_quantised_epilogue(splits, gemm_kind):
         q, s, _, _ = ops.quantize_act_1x128(C, rows=True, tokens=False)
         assert torch.equal(Cq, q), lay
         assert torch.equal(sCq.view(torch.int32), s.view(torch.int32)), lay
+        # ... and the oracle's codes of that same bf16 output, bit for bit
+        oq, os_ = quant.quantize_act_1x128(np32(C))
+        assert_codes_equal(u8(Cq), oq, lay + " Cq")
+        assert_scales_equal(sCq.cpu().numpy(), os_, lay + " sCq")
         # and they decode close to the oracle's output
         deq = (Cq.view(torch.float8_e4m3fn).float() * sCq.t().repeat_interleave(128, dim=1)).cpu().numpy()
         assert rel_fro(deq, want) < 0.05
