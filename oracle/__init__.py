@@ -27,6 +27,8 @@ quant   : the 1x128 activation quantiser (along features or along tokens) and
           the 128x128 weight quantiser, plus the per-tensor comparator.
 gemm    : the block-scaled GEMM with fp32 promotion per 128-deep slice for the
           fprop, dgrad and wgrad layouts, and the composed linear fwd/bwd.
+swiglu  : the SiLU-gated FFN activation h = bf16(SiLU(g) * u) that feeds the
+          down projection, and its 1x128 quantisation.
 
 Every floating-point step follows IEEE binary32 or binary64 through numpy;
 numpy never flushes subnormals.  Parity of every function is pinned by the
@@ -34,4 +36,4 @@ tests in ``tests/test_oracle_*.py`` against things other than the oracle
 itself (closed forms, library conversions, brute force, hand-worked cases).
 """
 
-from . import formats, quant, gemm  # noqa: F401
+from . import formats, quant, gemm, swiglu  # noqa: F401
