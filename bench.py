@@ -61,7 +61,7 @@ FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
 # once the kernels change the bench line reports null until a new capture is
 # recorded.
 TRAFFIC = {
-    "a9336dcb7b5c11e2": {"gemm": 231.6e6, "quant": 155.7e6},
+    "ad55d462807144a1": {"gemm": 232.3e6, "quant": 155.8e6},
 }
 
 
@@ -123,6 +123,8 @@ def parse_args(argv=None):
                     help="weights quantised once before the timed steps (cached across micro-steps)")
     ap.add_argument("--graph", action="store_true",
                     help="time the step as replays of a CUDA graph captured once (per-call rates from an eager pass)")
+    ap.add_argument("--probe-swiglu", action="store_true",
+                    help="time the SiLU-gated prologue (bfp8_swiglu_quantize_1x128) on the down projection's input")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
     return ap.parse_args(argv)
@@ -789,10 +791,56 @@ def fp8_peak_probe():
     return 0
 
 
+def swiglu_probe(args):
+    """The SiLU-gated prologue on the down projection's input, gate+up output
+    gu [8192, 12288] drawn as the mlp_down recipe (G, U ~ 0.5 t(4)): both
+    1x128 quantisations of h [8192, 6144], no copy of h.  CUDA events over 20
+    calls after 3 warm-up calls; the 201 MB input is larger than L2."""
+    import torch
+    from blockwise_fp8_linear_quantise_b300 import ops, workloads
+    wl = workloads.make("mlp_down")
+    gu = workloads.tensor(wl, "gu").to("cuda")
+    M, F = gu.shape[0], gu.shape[1] // 2
+    outs = ops.swiglu_quantize_1x128(gu, scale_mode=args.scale_mode)
+    call = lambda: ops.swiglu_quantize_1x128(gu, h=None, q=outs[1], s=outs[2], qT=outs[3], sT=outs[4],
+                                             scale_mode=args.scale_mode)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert ops.sync_status() == 0
+    clocks = ClockSampler(gpu_uuid(gu.device))
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = 20
+    e0.record()
+    for _ in range(n):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert ops.sync_status() == 0
+    us = e0.elapsed_time(e1) * 1e3 / n
+    per_elem = 4 + 2 + 8 / 128  # g and u read, two codes and two scales per 128 written
+    nbytes = M * F * per_elem
+    peaks, basis = load_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    line = {"probe": "swiglu_quantize_1x128", "workload": f"gu [{M}, {2 * F}] -> h [{M}, {F}], rows + tokens",
+            "scale_mode": args.scale_mode, "us_per_call": round(us, 2), "bytes_per_call": int(nbytes),
+            "value": round(gbs, 1), "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_basis": f"{basis} HBM copy", "clocks": clk,
+            "unfused_bytes_per_call": int(M * F * (per_elem + 4)),
+            "note": "unfused, h would be written and read back: 4 more bytes per element"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.probe_fp8_peak:
         return fp8_peak_probe()
+    if args.probe_swiglu:
+        return swiglu_probe(args)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

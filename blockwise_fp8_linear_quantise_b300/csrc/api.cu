@@ -68,12 +68,14 @@ bfp8_status device_state(DeviceState** out) {
     }
     cudaError_t e = cudaSuccess;
     // two quantiser CTAs per SM need the largest shared-memory carveout
-#define BFP8_SET_QUANT_SMEM(W, MODE, SCALE)                                                                     \
-  if (e == cudaSuccess)                                                                                          \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             kQuantSmemBytes);                                                                   \
-  if (e == cudaSuccess)                                                                                          \
-    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+#define BFP8_SET_QUANT_SMEM_GLU(W, MODE, SCALE, GLU, BYTES)                                               \
+  if (e == cudaSuccess)                                                                                     \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE, GLU>,                                     \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);                           \
+  if (e == cudaSuccess)                                                                                     \
+    e = cudaFuncSetAttribute(quantize_tile_kernel<W, MODE, SCALE, GLU>,                                     \
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+#define BFP8_SET_QUANT_SMEM(W, MODE, SCALE) BFP8_SET_QUANT_SMEM_GLU(W, MODE, SCALE, false, kQuantSmemBytes)
 #define BFP8_SET_QUANT_SMEM_ALL(SCALE)                  \
   BFP8_SET_QUANT_SMEM(false, kQRows, SCALE)             \
   BFP8_SET_QUANT_SMEM(false, kQCols, SCALE)             \
@@ -85,7 +87,17 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_SET_QUANT_SMEM_ALL(kScalePow2)
     BFP8_SET_QUANT_SMEM_ALL(kScaleMulRecip)
 #undef BFP8_SET_QUANT_SMEM_ALL
+    // the SiLU-gated prologue: one CTA per SM with two tiles per ring slot
+#define BFP8_SET_GLU_SMEM_ALL(SCALE)                                                      \
+  BFP8_SET_QUANT_SMEM_GLU(false, kQRows, SCALE, true, kQuantGluSmemBytes)                 \
+  BFP8_SET_QUANT_SMEM_GLU(false, kQCols, SCALE, true, kQuantGluSmemBytes)                 \
+  BFP8_SET_QUANT_SMEM_GLU(false, kQRows | kQCols, SCALE, true, kQuantGluSmemBytes)
+    BFP8_SET_GLU_SMEM_ALL(kScaleAmax448)
+    BFP8_SET_GLU_SMEM_ALL(kScalePow2)
+    BFP8_SET_GLU_SMEM_ALL(kScaleMulRecip)
+#undef BFP8_SET_GLU_SMEM_ALL
 #undef BFP8_SET_QUANT_SMEM
+#undef BFP8_SET_QUANT_SMEM_GLU
 #define BFP8_SET_GEMM_SMEM(BN, MODE, EPI)                                                                     \
   if (e == cudaSuccess)                                                                                        \
     e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
@@ -374,40 +386,47 @@ bfp8_status launch_gemm_pair(int mode, const CUtensorMap& ta, const CUtensorMap&
 // Persistent quantiser grid: two CTAs per SM (each streams its tiles
 // through a 3-deep shared-memory ring).  The tile walk and the TMA
 // coordinates are 32-bit: C up to 2^27 and fewer than 2^31 tiles.
-template <bool kWeight, int kScale>
+template <bool kWeight, int kScale, bool kGlu>
 bfp8_status launch_quant_mode(const CUtensorMap& tm, const QuantParams& p, unsigned grid, cudaStream_t st) {
+  constexpr int kSmem = kGlu ? kQuantGluSmemBytes : kQuantSmemBytes;
   const int mode = (p.q ? kQRows : 0) | (p.qT ? kQCols : 0);
   if (mode == kQRows)
-    quantize_tile_kernel<kWeight, kQRows, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows, kScale, kGlu><<<grid, kQuantThreads, kSmem, st>>>(tm, p);
   else if (mode == kQCols)
-    quantize_tile_kernel<kWeight, kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQCols, kScale, kGlu><<<grid, kQuantThreads, kSmem, st>>>(tm, p);
   else
-    quantize_tile_kernel<kWeight, kQRows | kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(tm, p);
+    quantize_tile_kernel<kWeight, kQRows | kQCols, kScale, kGlu><<<grid, kQuantThreads, kSmem, st>>>(tm, p);
   return BFP8_OK;
 }
 
-template <bool kWeight>
+template <bool kWeight, bool kGlu>
 bfp8_status launch_quant_scale(const CUtensorMap& tm, const QuantParams& p, unsigned grid, int scale_mode,
                                cudaStream_t st) {
-  if (scale_mode == kScalePow2) return launch_quant_mode<kWeight, kScalePow2>(tm, p, grid, st);
-  if (scale_mode == kScaleMulRecip) return launch_quant_mode<kWeight, kScaleMulRecip>(tm, p, grid, st);
-  return launch_quant_mode<kWeight, kScaleAmax448>(tm, p, grid, st);
+  if (scale_mode == kScalePow2) return launch_quant_mode<kWeight, kScalePow2, kGlu>(tm, p, grid, st);
+  if (scale_mode == kScaleMulRecip) return launch_quant_mode<kWeight, kScaleMulRecip, kGlu>(tm, p, grid, st);
+  return launch_quant_mode<kWeight, kScaleAmax448, kGlu>(tm, p, grid, st);
 }
 
-bfp8_status launch_quant(QuantParams p, bool weight, int scale_mode, cudaStream_t st) {
+// glu: p.x is the gate+up output [R, 2C] and the kernel quantises
+// h = bf16(SiLU(g) u) [R, C] (one CTA per SM; row length 2C up to 2^27).
+bfp8_status launch_quant(QuantParams p, bool weight, int scale_mode, cudaStream_t st, bool glu = false) {
   DeviceState* dev = nullptr;
   bfp8_status s = device_state(&dev);
   if (s != BFP8_OK) return s;
   if (p.q == nullptr && p.qT == nullptr) return BFP8_EINVAL;
+  if (glu && weight) return BFP8_EINVAL;
   const int64_t tiles = (p.R / 128) * (p.C / 128);
-  if (p.C > (int64_t(1) << 27) || tiles >= (int64_t(1) << 31)) return BFP8_EINVAL;
+  if (p.C > (int64_t(1) << (glu ? 26 : 27)) || tiles >= (int64_t(1) << 31)) return BFP8_EINVAL;
   p.ctiles = static_cast<uint32_t>(p.C / 128);
   p.tiles = static_cast<uint32_t>(tiles);
   CUtensorMap tm;
-  if ((s = make_quant_tmap(&tm, p.x, p.R, p.C)) != BFP8_OK) return s;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
-  s = weight ? launch_quant_scale<true>(tm, p, grid, scale_mode, st)
-             : launch_quant_scale<false>(tm, p, grid, scale_mode, st);
+  if ((s = make_quant_tmap(&tm, p.x, p.R, glu ? 2 * p.C : p.C)) != BFP8_OK) return s;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * (glu ? 1 : 2)));
+  if (glu)
+    s = launch_quant_scale<false, true>(tm, p, grid, scale_mode, st);
+  else
+    s = weight ? launch_quant_scale<true, false>(tm, p, grid, scale_mode, st)
+               : launch_quant_scale<false, false>(tm, p, grid, scale_mode, st);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -503,6 +522,23 @@ bfp8_status quant_act_impl(const void* x, int64_t M, int64_t K, uint8_t* q, floa
   if (st != BFP8_OK) return st;
   QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns, 0u, 0u};
   return launch_quant(p, false, scale_mode, stream);
+}
+
+bfp8_status swiglu_quant_impl(const void* gu, int64_t M, int64_t F, void* h, uint8_t* q, float* s, uint8_t* qT,
+                              float* sT, int scale_mode, cudaStream_t stream) {
+  if (!scale_mode_ok(scale_mode)) return BFP8_EINVAL;
+  if (!gu || (!q && !qT)) return BFP8_EINVAL;
+  if ((q && !s) || (qT && !sT)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(F)) return BFP8_EINVAL;
+  if (!aligned16(gu) || (h && !aligned16(h)) || (q && (!aligned16(q) || !aligned16(s))) ||
+      (qT && (!aligned16(qT) || !aligned16(sT))))
+    return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status st = device_state(&dev);
+  if (st != BFP8_OK) return st;
+  QuantParams p{static_cast<const uint16_t*>(gu), M, F, q, s, qT, sT, dev->wait_ns, 0u, 0u,
+                static_cast<uint16_t*>(h)};
+  return launch_quant(p, false, scale_mode, stream, true);
 }
 
 bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s, int scale_mode,
@@ -653,6 +689,11 @@ bfp8_status bfp8_quantize_act_1x128_ex(const void* x, int64_t M, int64_t K, uint
 bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s,
                                        bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
   return quant_w_impl(w, N, K, q, qT, s, scale_mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_swiglu_quantize_1x128(const void* gu, int64_t M, int64_t F, void* h, uint8_t* q, float* s,
+                                       uint8_t* qT, float* sT, bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
+  return swiglu_quant_impl(gu, M, F, h, q, s, qT, sT, scale_mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bfp8_status bfp8_fp8_block_gemm(bfp8_layout layout, const uint8_t* A, const float* sa, const uint8_t* B,

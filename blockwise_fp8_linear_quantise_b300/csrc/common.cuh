@@ -368,6 +368,62 @@ __device__ __forceinline__ uint32_t quant_pair(float a, float b, const GroupScal
   return quant_pair_div(a, b, g.s, g.s);
 }
 
+// ---- SiLU-gated FFN activation, h = SiLU(g) u = g u / (1 + e^-g) ----------
+// The down projection of the FFN takes h, a bf16 tensor; its quantiser can
+// form h itself from the gate+up output.  e^-|g| = 2^(-|g| log2 e) comes from
+// the PTX instruction ex2.approx.f32 (relative error about 2^-22, subnormal
+// results kept) and 1 / (1 + e^-|g|) from rcp.approx.ftz.f32 on [1, 2], so h
+// is within a few fp32 ulp of the exact value before its bf16 rounding.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// SiLU(g) u for |g| <= 64, where p = e^-|g| >= 2^-93 is a normal fp32:
+// sigma(g) = 1 / (1 + p) for g >= 0 and p / (1 + p) for g < 0.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  const float p = ex2_approx(fabsf(g) * -kLog2e);
+  const float r = rcp_approx(1.0f + p);
+  return (g * u) * (g < 0.0f ? p * r : r);
+}
+
+// The same for any finite g.  Beyond |g| = 64, 1 + e^-|g| rounds to 1, and
+// for g < 0 the factor e^-|g| is formed as 2^64 e^-|g| (a normal fp32 down to
+// |g| of about 131) and the 2^-64 is applied last, so h keeps its precision
+// until it is itself below the fp32 normal range.
+__device__ __forceinline__ float silu_mul_wide(float g, float u) {
+  const float a = fabsf(g);
+  const bool big = a > 64.0f;
+  const float p = ex2_approx(fmaf(a, -kLog2e, big ? 64.0f : 0.0f));
+  const float r = rcp_approx(1.0f + (big ? 0.0f : p));
+  const float h = (g * u) * (g < 0.0f ? p * r : r);
+  return (big && g < 0.0f) ? h * 0x1p-64f : h;
+}
+
+// bf16_rn(SiLU(g) u) for the two bf16 values of each word (low half first).
+template <bool kWide>
+__device__ __forceinline__ uint32_t swiglu_bf16x2(uint32_t g, uint32_t u) {
+  const float lo = kWide ? silu_mul_wide(bf16lo(g), bf16lo(u)) : silu_mul(bf16lo(g), bf16lo(u));
+  const float hi = kWide ? silu_mul_wide(bf16hi(g), bf16hi(u)) : silu_mul(bf16hi(g), bf16hi(u));
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h2);
+}
+
+template <bool kWide>
+__device__ __forceinline__ uint4 swiglu_bf16x8(const uint4& g, const uint4& u) {
+  return make_uint4(swiglu_bf16x2<kWide>(g.x, u.x), swiglu_bf16x2<kWide>(g.y, u.y), swiglu_bf16x2<kWide>(g.z, u.z),
+                    swiglu_bf16x2<kWide>(g.w, u.w));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -49,14 +49,15 @@
 namespace bfp8 {
 
 struct QuantParams {
-  const uint16_t* x;  // bf16 [R, C]
-  int64_t R, C;
+  const uint16_t* x;  // bf16 [R, C]; for the SiLU-gated prologue [R, 2C] = [g || u]
+  int64_t R, C;       // the quantised tensor (h for the prologue)
   uint8_t* q;   // [R, C] or null
   float* s;     // act: [C/128, R];  weight: [R/128, C/128]
   uint8_t* qT;  // [C, R] or null
   float* sT;    // act: [R/128, C];  unused for weights
   uint64_t wait_ns;
   uint32_t ctiles, tiles;  // C/128 and (R/128)(C/128), filled in by the launcher
+  uint16_t* h;             // prologue only: bf16 [R, C] copy of h, or null
 };
 
 // Which outputs a kernel instance writes (a template bit set).
@@ -66,10 +67,20 @@ constexpr int kQCols = 2;  // qT (, sT): groups along the rows, stored transpose
 constexpr int kQComputeWarps = 8;
 constexpr int kQuantThreads = 32 * kQComputeWarps;
 constexpr int kQStages = 3;
-constexpr int kQTileBytes = 128 * 256;                       // bf16 tile, also the ring slot
-constexpr int kQBarOff = kQStages * kQTileBytes;             // full[3], empty[3], redbar[2]
-constexpr int kQRedOff = kQBarOff + (2 * kQStages + 2) * 8;  // float[2][8] (weight block amax)
-constexpr int kQuantSmemBytes = kQRedOff + 2 * kQComputeWarps * 4 + 1024;  // + room to align to 1024
+constexpr int kQTileBytes = 128 * 256;  // bf16 tile
+
+// Shared memory: the ring (one tile per slot, or the g and u tiles of the
+// SiLU-gated prologue), then full[3], empty[3], redbar[2] and float[2][8]
+// (weight block amax), plus room to align the base to 1024.
+template <bool kGlu>
+struct QuantLayout {
+  static constexpr int kSlot = (kGlu ? 2 : 1) * kQTileBytes;
+  static constexpr int kBarOff = kQStages * kSlot;
+  static constexpr int kRedOff = kBarOff + (2 * kQStages + 2) * 8;
+  static constexpr int kSmemBytes = kRedOff + 2 * kQComputeWarps * 4 + 1024;
+};
+constexpr int kQuantSmemBytes = QuantLayout<false>::kSmemBytes;
+constexpr int kQuantGluSmemBytes = QuantLayout<true>::kSmemBytes;
 
 // Tile coordinates of a persistent CTA's walk (tile t = rt * ctiles + ct).
 struct TileWalk {
@@ -152,14 +163,20 @@ __device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupSc
 }
 
 // Warp 0 fetches tile (rt, ct) into ring slot `buf` with 32 TMA boxes (one
-// per lane; lane 0 arms the slot's barrier first).
-__device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t C, uint32_t rt, uint32_t ct, uint8_t* buf,
-                                           uint64_t* bar, int lane) {
-  if (lane == 0) mbar_arrive_expect_tx(bar, kQTileBytes);
+// per lane; lane 0 arms the slot's barrier first).  xrow is the input's row
+// length.  The SiLU-gated prologue also fetches the u tile, uoff columns to
+// the right, into the slot's second half.
+template <bool kGlu>
+__device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t xrow, uint32_t uoff, uint32_t rt,
+                                           uint32_t ct, uint8_t* buf, uint64_t* bar, int lane) {
+  if (lane == 0) mbar_arrive_expect_tx(bar, QuantLayout<kGlu>::kSlot);
   __syncwarp();
   const int l = lane >> 1, h = lane & 1;
-  tma_load_2d(buf + 16384 * h + 1024 * l, tmx, static_cast<int32_t>(l * C + ct * 128 + 64 * h),
-              static_cast<int32_t>(rt * 8), bar);
+  const int32_t x0 = static_cast<int32_t>(l * xrow + ct * 128 + 64 * h);
+  tma_load_2d(buf + 16384 * h + 1024 * l, tmx, x0, static_cast<int32_t>(rt * 8), bar);
+  if constexpr (kGlu)
+    tma_load_2d(buf + kQTileBytes + 16384 * h + 1024 * l, tmx, x0 + static_cast<int32_t>(uoff),
+                static_cast<int32_t>(rt * 8), bar);
 }
 
 // Codes of this warp's row and column slices of one tile, stored to global
@@ -188,19 +205,27 @@ __device__ __forceinline__ void quant_tile_codes(const uint4 (&rv)[8], const uin
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
 // kWeight = true : one 128x128 block per tile (q and/or qT, one scale).
 // kScale: the scale mode (kScaleAmax448, kScalePow2 or kScaleMulRecip).
-template <bool kWeight, int kMode, int kScale>
-__global__ void __launch_bounds__(kQuantThreads, 2)
+// kGlu: the input is the gate+up output [g || u] and the quantised tensor is
+// h = bf16_rn(SiLU(g) u) (the down projection's activation).  Each warp forms
+// h for its 16 rows, writes it over g in the slot (and to p.h if given), and
+// the column view reads h once every warp's rows are in place (redbar, all
+// 256 threads arriving).  One CTA per SM: a slot holds two tiles.
+template <bool kWeight, int kMode, int kScale, bool kGlu>
+__global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
+  static_assert(!(kGlu && kWeight), "the SiLU-gated prologue quantises an activation");
+  using L = QuantLayout<kGlu>;
   constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQBarOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + kQStages;
-  uint64_t* redbar = empty + kQStages;  // weight block amax exchange, by tile parity
-  float* red = reinterpret_cast<float*>(smem + kQRedOff);
+  uint64_t* redbar = empty + kQStages;  // weight block amax / prologue h exchange, by tile parity
+  float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ctiles = p.ctiles, tiles = p.tiles, C = static_cast<uint32_t>(p.C);
+  const uint32_t xrow = kGlu ? 2u * C : C;  // input row length
   const uint32_t step = gridDim.x, drt = step / ctiles, dct = step % ctiles;
 
   if (threadIdx.x == 0) {
@@ -208,8 +233,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kQComputeWarps);
     }
-    mbar_init(&redbar[0], kQComputeWarps);
-    mbar_init(&redbar[1], kQComputeWarps);
+    mbar_init(&redbar[0], kGlu ? kQuantThreads : kQComputeWarps);
+    mbar_init(&redbar[1], kGlu ? kQuantThreads : kQComputeWarps);
     fence_mbar_init();
   }
   __syncthreads();
@@ -221,7 +246,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   uint32_t issued = 0;  // tiles of this CTA issued so far (warp 0)
   if (warp == 0) {
     for (; issued < kQStages && fill.t < tiles; ++issued) {
-      quant_fill(&tmx, C, fill.rt, fill.ct, smem + issued * kQTileBytes, &full[issued], lane);
+      quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + issued * L::kSlot, &full[issued], lane);
       fill.advance(step, drt, dct, ctiles);
     }
   }
@@ -245,18 +270,61 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   for (; cur.t < tiles; cur.advance(step, drt, dct, ctiles), ++j) {
     const uint32_t s = j % kQStages, ph = (j / kQStages) & 1u;
     if (!mbar_wait(&full[s], ph, p.wait_ns, kWeight ? 0x201u : 0x101u)) break;
-    const uint8_t* buf = smem + s * kQTileBytes;
+    uint8_t* buf = smem + s * L::kSlot;
     const int64_t r0 = static_cast<int64_t>(cur.rt) * 128, c0 = static_cast<int64_t>(cur.ct) * 128;
 
     // both slices into registers, then hand the slot back
     uint4 rv[8];
     uint2 cv[16];
-    if constexpr (kRows) {
+    if constexpr (kRows || kGlu) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         rv[2 * m] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1))));
         rv[2 * m + 1] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1) + 16u)));
       }
+    }
+    if constexpr (kGlu) {
+      // h for this warp's rows: the u row slice sits at the same offsets in
+      // the slot's second half.  The exponent path is chosen per warp: the
+      // wide one only when some |g| of the slice exceeds 64.
+      uint4 ru[8];
+      uint32_t gm2 = 0u;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint8_t* ub = buf + kQTileBytes + 16384 * (m >> 1);
+        ru[2 * m] = *reinterpret_cast<const uint4*>(ub + (roff ^ (64u * (m & 1))));
+        ru[2 * m + 1] = *reinterpret_cast<const uint4*>(ub + (roff ^ (64u * (m & 1) + 16u)));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        gm2 = bf16x2_maxabs(bf16x2_maxabs(gm2, bf16x2_maxabs(rv[k].x, rv[k].y)), bf16x2_maxabs(rv[k].z, rv[k].w));
+      if (__any_sync(0xffffffffu, !(bf16x2_absmax(gm2) <= 64.0f))) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rv[k] = swiglu_bf16x8<true>(rv[k], ru[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rv[k] = swiglu_bf16x8<false>(rv[k], ru[k]);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        *reinterpret_cast<uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1)))) = rv[2 * m];
+        *reinterpret_cast<uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1) + 16u))) = rv[2 * m + 1];
+      }
+      if (p.h != nullptr) {
+        // chunks 4m + 2h + u of the row: columns 32m + 16h + 8u
+        uint16_t* hrow = p.h + (static_cast<int64_t>(r0) + wrow) * p.C + c0 + 16 * hh;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          *reinterpret_cast<uint4*>(hrow + 32 * m) = rv[2 * m];
+          *reinterpret_cast<uint4*>(hrow + 32 * m + 8) = rv[2 * m + 1];
+        }
+      }
+      // The slot is refilled by TMA after every warp releases it: order these
+      // generic-proxy writes before that async-proxy write, and release them
+      // to the other warps (each thread arrives for its own writes).
+      fence_proxy_async_smem();
+      mbar_arrive(&redbar[j & 1u]);
+      if (!mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, p.wait_ns, 0x131u)) break;
     }
     if constexpr (kCols) {
 #pragma unroll
@@ -271,7 +339,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      quant_fill(&tmx, C, fill.rt, fill.ct, smem + sf * kQTileBytes, &full[sf], lane);
+      quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + sf * L::kSlot, &full[sf], lane);
       fill.advance(step, drt, dct, ctiles);
       ++issued;
     }

@@ -94,6 +94,38 @@ def quantize_act_1x128(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=N
     return q, s, qT, sT
 
 
+def swiglu_quantize_1x128(gu, rows=True, tokens=True, want_h=False, h=None, q=None, s=None, qT=None, sT=None,
+                          stream=None, scale_mode="amax448"):
+    """The down projection's input from the gate+up output gu [M, 2F] (gate in
+    columns 0..F-1, up in F..2F-1): h = bf16(SiLU(g) * u), quantised in 1x128
+    groups as quantize_act_1x128(h, rows, tokens) does, in one pass.
+
+    Returns (h or None, q, s, qT, sT); h [M, F] bf16 is written only when
+    want_h (or h) is given.
+    """
+    M, F2 = gu.shape
+    _need(gu, torch.bfloat16, (M, F2), "gu")
+    if F2 % 2:
+        raise ValueError("gu must have an even number of columns")
+    F = F2 // 2
+    h = _out(h, torch.bfloat16, (M, F), gu.device, "h") if (want_h or h is not None) else None
+    if rows:
+        q = _out(q, torch.uint8, (M, F), gu.device, "q")
+        s = _out(s, torch.float32, (F // 128, M), gu.device, "s")
+    else:
+        q = s = None
+    if tokens:
+        qT = _out(qT, torch.uint8, (F, M), gu.device, "qT")
+        sT = _out(sT, torch.float32, (M // 128, F), gu.device, "sT")
+    else:
+        qT = sT = None
+    lib = _lib.load()
+    _check(lib.bfp8_swiglu_quantize_1x128(_ptr(gu), M, F, _ptr(h), _ptr(q), _ptr(s), _ptr(qT), _ptr(sT),
+                                          _scale_mode(scale_mode), _stream(stream)),
+           "swiglu_quantize_1x128")
+    return h, q, s, qT, sT
+
+
 def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, stream=None, scale_mode="amax448"):
     """Quantise bf16 w [N, K] in 128x128 blocks -> (q [N, K], qT [K, N], s [N/128, K/128]).
 

@@ -16,6 +16,8 @@ Workloads (name -> what it is):
 * ``mlp_gateup`` X [8192, 2048] ~ N(0,1) with 0.1% x30, W [12288, 2048] (gate || up) ~ N(0, 0.02^2); fprop.
 * ``mlp_down``   X [8192, 6144] = SiLU(G) * U with G, U ~ 0.5 * Student-t(nu=4),
                  W [2048, 6144] ~ N(0, (0.02/sqrt(56))^2), dY [8192, 2048] ~ N(0, 1e-3^2); fprop, dgrad, wgrad.
+                 ``gu`` [8192, 12288] = [G || U] itself, the gate+up output that the SiLU-gated
+                 prologue turns into the down projection's input.
 * ``attn_proj``  X [16384, 2048] ~ Student-t(nu=3) shared by QKV W [4096, 2048] and O W [2048, 2048]
                  ~ N(0, 0.02^2); dY [16384, 4096] and [16384, 2048] ~ N(0, 1e-3^2); all three layouts.
 * ``stack28``    28 layers x {QKV 2048->4096, O 2048->2048, gate+up 2048->12288, down 6144->2048}
@@ -152,8 +154,9 @@ def make(name):
         M, N, K = TOKENS_8K, 2048, 6144
         wl = Workload(name, 3, [LinearSpec("down", M, N, K, "x", "w", "dy", True)])
         wl.dists = {"x": Dist("silu_gated_t", 0.5, nu=4.0),
-                    "w": Dist("normal", 0.02 / math.sqrt(2 * 28)), "dy": DY}
-        wl.shapes = {"x": (M, K), "w": (N, K), "dy": (M, N)}
+                    "w": Dist("normal", 0.02 / math.sqrt(2 * 28)), "dy": DY,
+                    "gu": Dist("student_t", 0.5, nu=4.0)}
+        wl.shapes = {"x": (M, K), "w": (N, K), "dy": (M, N), "gu": (M, 2 * K)}
     elif name == "attn_proj":
         M = TOKENS_16K
         wl = Workload(name, 4, [

@@ -136,6 +136,28 @@ bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K,
                                        bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
+ * SiLU-gated FFN activation fused into the activation quantiser: the input of
+ * the FFN's down projection, h = bf16_rn(SiLU(g) * u) with
+ * SiLU(g) = g / (1 + e^-g), is formed from the fused gate+up output and
+ * quantised in 1x128 groups without a round trip through HBM ("Puro-2B ...",
+ * section 3.2: the activation stays BF16 and FP8 is the linear layers' operand
+ * format; the tutorial's model-architecture paragraph: FFN width 6144).
+ *
+ *   gu  bf16 [M, 2F], read only: gate g in columns 0..F-1, up u in F..2F-1.
+ *   h   bf16 [M, F] or NULL: a copy of h (not needed by the down projection).
+ *   q, s, qT, sT  as bfp8_quantize_act_1x128 for x = h [M, F] (K = F).
+ * M and F positive multiples of 128, F at most 2^26.  h is computed in fp32
+ * with the hardware 2^x and 1/x approximations (relative error about 2^-22)
+ * and rounded to bf16 once, so it can differ from the exactly rounded value by
+ * one bf16 unit where the product lies that close to a rounding midpoint;
+ * the codes are the scale_mode quantisation of this h, bit for bit.  At least
+ * one of q / qT must be given.  Errors: EINVAL, EALIGN, ECUDA.
+ */
+bfp8_status bfp8_swiglu_quantize_1x128(const void* gu, int64_t M, int64_t F, void* h,
+                                       uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                       bfp8_scale_mode scale_mode, bfp8_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM with fp32 promotion per 128-deep slice (section 3.2:
  * E4M3 operands, fp32 training state; scales per 1x128 group / 128x128 block).
  *

@@ -76,6 +76,20 @@ def test_quantize_rejects_nulls_and_misalignment():
     assert lib.bfp8_quantize_w_128x128(FAKE, 128, 128, FAKE, MIS, FAKE, None) == EALIGN
 
 
+def test_swiglu_quantize_rejects_bad_arguments():
+    f = _lib.load().bfp8_swiglu_quantize_1x128
+    assert f(None, 128, 128, None, FAKE, FAKE, None, None, 0, None) == EINVAL
+    assert f(FAKE, 128, 128, FAKE, None, None, None, None, 0, None) == EINVAL  # no codes requested
+    assert f(FAKE, 128, 128, None, FAKE, None, None, None, 0, None) == EINVAL  # q without s
+    assert f(FAKE, 128, 128, None, None, None, FAKE, None, 0, None) == EINVAL  # qT without sT
+    assert f(FAKE, 128, 100, None, FAKE, FAKE, None, None, 0, None) == EINVAL
+    assert f(FAKE, 0, 128, None, FAKE, FAKE, None, None, 0, None) == EINVAL
+    assert f(FAKE, 128, 128, None, FAKE, FAKE, None, None, 5, None) == EINVAL
+    assert f(MIS, 128, 128, None, FAKE, FAKE, None, None, 0, None) == EALIGN
+    assert f(FAKE, 128, 128, MIS, FAKE, FAKE, None, None, 0, None) == EALIGN
+    assert f(FAKE, 128, 128, None, FAKE, FAKE, MIS, FAKE, 0, None) == EALIGN
+
+
 def test_gemm_rejects_bad_arguments():
     lib = _lib.load()
     g = lib.bfp8_fp8_block_gemm
