@@ -1,4 +1,4 @@
-"""The kernels' division-free quotient, checked exhaustively on the CPU.
+"""The kernels' division-free quotient and scales, checked exhaustively on the CPU.
 
 The GPU quantisers (amax/448 mode) form fp32_rn(x / s) without a division:
 r = RN(1/s) once per group, y0 = RN(x r), then one FMA correction
@@ -14,6 +14,11 @@ one float64 rounding that is not) and requires Q == fp32(x / s) bit for bit.
 
 No oracle and no GPU code is used: the scheme is restated from the kernels'
 header comment, and the reference quotient is numpy's IEEE float32 division.
+
+Two per-group steps are checked the same way, over every positive bf16 amax:
+the amax/448 scale (one FMA correction of RN(amax RN(1/448))) against the
+IEEE quotient, and the power-of-two mode's exponent read off amax's bits
+against an exact rational search.
 """
 
 import numpy as np
@@ -123,3 +128,51 @@ def _e4m3_index(v):
 def _e4m3_mag(c):
     e, m = c >> 3, c & 7
     return m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+
+
+def _positive_bf16():
+    return (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+
+
+def test_amax_scale_by_one_correction_is_the_ieee_quotient():
+    """s = RN(amax / 448) as the kernels form it for a bf16 amax with a normal
+    quotient: q0 = RN(amax c) with c = RN(1/448), then RN(q0 + c RN(amax - 448 q0))."""
+    amax = _positive_bf16()
+    amax = amax[(amax >= np.float32(448.0 * 2.0 ** -126)) & (amax <= np.float32(float.fromhex("0x1.FEp+127")))]
+    c = np.float32(1.0) / np.float32(448.0)
+    q0 = amax * c
+    r = _fma32_exact(-q0, np.full_like(q0, 448.0), amax)
+    s = _fma32_exact(r, np.full_like(r, c), q0)
+    want = amax / np.float32(448.0)
+    assert amax.size == 31392  # every positive bf16 amax whose quotient is a normal fp32
+    assert np.array_equal(s.view(np.uint32), want.view(np.uint32))
+
+
+def _pow2_k_from_bits(amax):
+    """The kernels' exponent of the power-of-two scale, from amax's bits:
+    amax = (1 + m) 2^e (fp32 subnormals normalised), k = e - 8 + (m > 0.75)."""
+    b = amax.view(np.uint32).astype(np.int64)
+    normal = b >= 0x00800000
+    e = np.where(normal, (b >> 23) - 127, 0)
+    m = np.where(normal, b & 0x007FFFFF, 0)
+    sub = ~normal
+    if np.any(sub):
+        bs = b[sub]
+        p = np.floor(np.log2(bs.astype(np.float64))).astype(np.int64)  # exact for integers below 2^23
+        e[sub] = p - 149
+        m[sub] = (bs << (23 - p)) & 0x007FFFFF
+    return e - 8 + (m > 0x00600000)
+
+
+def test_pow2_exponent_from_bits_is_the_smallest_covering_power():
+    from fractions import Fraction as F
+    amax = _positive_bf16()
+    extra = (np.arange(1, 1 << 12, 7, dtype=np.uint32)).view(np.float32)  # fp32 subnormal amaxes
+    amax = np.concatenate([amax, extra])
+    k = _pow2_k_from_bits(amax)
+    # 2^k >= amax/448 > 2^(k-1), in exact float64 products (448 * 2^k is exact)
+    a64 = amax.astype(np.float64)
+    assert np.all(448.0 * np.ldexp(1.0, k) >= a64) and np.all(448.0 * np.ldexp(1.0, k - 1) < a64)
+    for a, kv in zip(amax[::97], k[::97]):  # exact rationals on a stride
+        fa = F(float(a))
+        assert F(2) ** int(kv) * 448 >= fa > F(2) ** (int(kv) - 1) * 448
