@@ -29,6 +29,8 @@ gemm    : the block-scaled GEMM with fp32 promotion per 128-deep slice for the
           fprop, dgrad and wgrad layouts, and the composed linear fwd/bwd.
 swiglu  : the SiLU-gated FFN activation h = bf16(SiLU(g) * u) that feeds the
           down projection, and its 1x128 quantisation.
+mx      : the MXFP8 1x32 recipe (power-of-two scales per 32 values along every
+          reduction, promotion per 32-deep slice), the comparison workload.
 
 Every floating-point step follows IEEE binary32 or binary64 through numpy;
 numpy never flushes subnormals.  Parity of every function is pinned by the
@@ -36,4 +38,4 @@ tests in ``tests/test_oracle_*.py`` against things other than the oracle
 itself (closed forms, library conversions, brute force, hand-worked cases).
 """
 
-from . import formats, quant, gemm, swiglu  # noqa: F401
+from . import formats, quant, gemm, swiglu, mx  # noqa: F401
