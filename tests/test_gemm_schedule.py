@@ -9,7 +9,10 @@ Puro-2B shapes and the small test shapes, with automatic and forced splits:
 * tiles stay inside the output, and consecutive units walk down a band of
   group_m m-tiles before moving to the next column of tiles (the L2 raster);
 * the persistent grid's strided walk (CTA b takes units b, b + grid, ...)
-  hands every unit to exactly one CTA (or CTA pair).
+  hands every unit to exactly one CTA (or CTA pair);
+* the shared-memory carve-up of each kernel instance keeps its TMA tiles and
+  staging 1024-byte aligned, its scale ring 16-byte aligned and its barriers
+  8-byte aligned, and fits the per-CTA limit and the TMEM columns.
 """
 
 import math
@@ -115,3 +118,35 @@ def test_the_stack_shapes_need_no_split():
     # every GEMM of the 16384-token stack fills the GPU with whole tiles
     for layout, M, N, K in gemms()[:12]:
         assert plan(layout, M, N, K)["splits"] == 1, (layout, M, N, K)
+
+
+def gemm_smem(pair, bn):
+    """The GEMM's shared-memory carve-up, restated from GemmSmem."""
+    stages = 4 if pair else (3 if bn == 256 else 4)
+    a_bytes = 128 * 128
+    b_bytes = (bn // 2 if pair else bn) * 128
+    b_off = stages * a_bytes
+    c_warp = 32 * (bn // 2) * 2
+    c_off = b_off + stages * b_bytes
+    slots, slot_floats = 8, 128 + bn
+    scale_off = c_off + 8 * c_warp
+    bar_off = scale_off + slots * slot_floats * 4
+    bars = 2 * stages + 5 + 2 * slots
+    tmem_slot = bar_off + bars * 8
+    return dict(stages=stages, a_bytes=a_bytes, b_bytes=b_bytes, b_off=b_off, c_off=c_off, c_warp=c_warp,
+                scale_off=scale_off, slot_bytes=slot_floats * 4, bar_off=bar_off, tmem_slot=tmem_slot,
+                alloc=tmem_slot + 16 + 1024, tmem_cols=2 * bn)
+
+
+def test_gemm_shared_memory_is_aligned_and_fits():
+    for pair, bn in ((True, 256), (False, 256), (False, 128)):
+        g = gemm_smem(pair, bn)
+        # 128-byte-swizzled TMA tiles and the epilogue staging start on 1024-byte boundaries
+        for s in range(g["stages"]):
+            assert (s * g["a_bytes"]) % 1024 == 0 and (g["b_off"] + s * g["b_bytes"]) % 1024 == 0
+        assert g["c_off"] % 1024 == 0 and g["c_warp"] % 1024 == 0
+        # the scale ring takes 16-byte cp.async copies; barriers are 8-byte words
+        assert g["scale_off"] % 16 == 0 and g["slot_bytes"] % 16 == 0
+        assert g["bar_off"] % 8 == 0 and g["tmem_slot"] % 4 == 0
+        assert g["alloc"] <= 232448                  # the per-CTA dynamic shared-memory limit
+        assert g["tmem_cols"] <= 512 and g["tmem_cols"] & (g["tmem_cols"] - 1) == 0  # power of two, <= 512
