@@ -37,6 +37,7 @@ SIGNATURES = {
     "bfp8_set_gemm_kernel": (c_int, [c_int]),
     "bfp8_set_gemm_splits": (c_int, [c_int]),
     "bfp8_launch_count": (ctypes.c_uint64, []),
+    "bfp8_test_stall_next_launch": (c_int, []),
     "bfp8_status_string": (ctypes.c_char_p, [c_int]),
 }
 

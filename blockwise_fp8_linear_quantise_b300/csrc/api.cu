@@ -34,9 +34,14 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-int g_forced_splits = 0;  // 0 = automatic
-int g_gemm_kind = 0;       // 0 = CTA pairs where the shape allows, 1 = single-CTA tiles only
+// Process-wide tuning knobs: read by every planning call, possibly from
+// several host threads at once, so they are atomics.
+std::atomic<int> g_forced_splits{0};  // 0 = automatic
+std::atomic<int> g_gemm_kind{0};      // 0 = CTA pairs where the shape allows, 1 = single-CTA tiles only
 std::atomic<uint64_t> g_launches{0};  // kernels launched by this library
+std::atomic<int> g_stall_next{0};     // test hook: the next quantiser or GEMM launch stalls (bounded)
+
+uint32_t take_stall() { return g_stall_next.exchange(0, std::memory_order_relaxed) != 0 ? 1u : 0u; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -101,7 +106,7 @@ bfp8_status device_state(DeviceState** out) {
 #define BFP8_SET_GEMM_SMEM(BN, MODE, EPI)                                                                     \
   if (e == cudaSuccess)                                                                                        \
     e = cudaFuncSetAttribute(block_gemm_kernel<BN, MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             GemmSmem<BN>::kAlloc);
+                             gemm_smem_alloc<BN, false, MODE, EPI>());
     BFP8_SET_GEMM_SMEM(256, kSbBlock, kEpiPlain)
     BFP8_SET_GEMM_SMEM(256, kSbBlockT, kEpiPlain)
     BFP8_SET_GEMM_SMEM(256, kSbCol, kEpiPlain)
@@ -121,7 +126,7 @@ bfp8_status device_state(DeviceState** out) {
 #define BFP8_SET_PAIR_SMEM(MODE, EPI)                                                                        \
   if (e == cudaSuccess)                                                                                       \
     e = cudaFuncSetAttribute(block_gemm_pair_kernel<MODE, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             GemmSmem<256, true>::kAlloc);
+                             gemm_smem_alloc<256, true, MODE, EPI>());
     BFP8_SET_PAIR_SMEM(kSbBlock, kEpiPlain)
     BFP8_SET_PAIR_SMEM(kSbBlockT, kEpiPlain)
     BFP8_SET_PAIR_SMEM(kSbCol, kEpiPlain)
@@ -181,7 +186,7 @@ bfp8_status device_state(DeviceState** out) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(sms - (sms & 1)), 1, 1);
       cfg.blockDim = dim3(kGemmThreads, 1, 1);
-      cfg.dynamicSmemBytes = GemmSmem<256, true>::kAlloc;
+      cfg.dynamicSmemBytes = gemm_smem_alloc<256, true, kSbBlock, kEpiPlain>();
       cudaLaunchAttribute attr;
       attr.id = cudaLaunchAttributeClusterDimension;
       attr.val.clusterDim.x = 2;
@@ -236,29 +241,32 @@ bfp8_status make_quant_tmap(CUtensorMap* map, const void* x, int64_t R, int64_t 
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
 }
 
-// fp32 [rows, cols] accumulation target, box 32 columns x 32 rows, 128-byte
-// swizzle (the accumulate epilogue's staging layout).
-bfp8_status make_f32_acc_tmap(CUtensorMap* map, float* base, int64_t rows, int64_t cols) {
+// The GEMM epilogue's output tensor maps: 32-row boxes of one 128-byte
+// swizzled row each (row layout), or of one 64-byte swizzled row each (the
+// column layout's 2 KB staging areas).
+//   fp32 [rows, cols] accumulation target: 32 (row layout) or 16 columns;
+//   bf16 [rows, cols] output: 64 (row layout) or 32 columns.
+bfp8_status make_f32_acc_tmap(CUtensorMap* map, float* base, int64_t rows, int64_t cols, bool col_layout) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {col_layout ? 16u : 32u, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        col_layout ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
 }
 
-// bf16 [rows, cols] output, box 64 columns x 32 rows, 128-byte swizzle (the
-// GEMM epilogue's staging layout).
-bfp8_status make_bf16_store_tmap(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
+bfp8_status make_bf16_store_tmap(CUtensorMap* map, void* base, int64_t rows, int64_t cols, bool col_layout) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, 32};
+  cuuint32_t box[2] = {col_layout ? 32u : 64u, 32};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        col_layout ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BFP8_OK : BFP8_ECUDA;
 }
 
@@ -279,7 +287,10 @@ struct GemmPlan {
 // with nominal B300 rates.
 GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const DeviceState& d) {
   GemmPlan g;
-  g.pair = g_gemm_kind == 0 && layout != BFP8_WGRAD && d.pair_clusters > 0 && M % 256 == 0 && N % 256 == 0;
+  const int forced_splits = g_forced_splits.load(std::memory_order_relaxed);
+  const int kind = g_gemm_kind.load(std::memory_order_relaxed);
+  g.pair = kind != 1 && (layout != BFP8_WGRAD || kind == 2) && d.pair_clusters > 0 && M % 256 == 0 &&
+           N % 256 == 0;
   g.bn = (N % 256 == 0) ? 256 : 128;
   g.m_tiles = static_cast<int>(M / (g.pair ? 256 : 128));
   g.n_tiles = static_cast<int>(N / g.bn);
@@ -287,8 +298,8 @@ GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const De
   g.slots = g.pair ? d.pair_clusters : d.sms;
   const int nk = static_cast<int>(K / 128);
   int best = 1;
-  if (g_forced_splits > 0) {
-    best = std::min(g_forced_splits, nk);
+  if (forced_splits > 0) {
+    best = std::min(forced_splits, nk);
   } else if (g.slots > 0) {
     const double t_gemm = 2.0 * M * N * K / 4.0e15;
     double best_t = 1e30;
@@ -312,16 +323,18 @@ GemmPlan plan_gemm(bfp8_layout layout, int64_t M, int64_t N, int64_t K, const De
 template <int BN, int kEpi>
 void launch_gemm_bn_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const GemmParams& p, int grid, cudaStream_t st) {
-  const int smem = GemmSmem<BN>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_kernel<BN, kSbBlock, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlock, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<BN, false, kSbBlock, kEpi>(), st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_kernel<BN, kSbBlockT, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbBlockT, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<BN, false, kSbBlockT, kEpi>(), st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_kernel<BN, kSbCol, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_kernel<BN, kSbCol, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<BN, false, kSbCol, kEpi>(), st>>>(ta, tb, tc, p);
       break;
   }
 }
@@ -356,16 +369,18 @@ bfp8_status launch_gemm_bn(int mode, const CUtensorMap& ta, const CUtensorMap& t
 template <int kEpi>
 void launch_gemm_pair_mode(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                            const GemmParams& p, int grid, cudaStream_t st) {
-  const int smem = GemmSmem<256, true>::kAlloc;
   switch (mode) {
     case kSbBlock:
-      block_gemm_pair_kernel<kSbBlock, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlock, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<256, true, kSbBlock, kEpi>(), st>>>(ta, tb, tc, p);
       break;
     case kSbBlockT:
-      block_gemm_pair_kernel<kSbBlockT, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbBlockT, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<256, true, kSbBlockT, kEpi>(), st>>>(ta, tb, tc, p);
       break;
     default:
-      block_gemm_pair_kernel<kSbCol, kEpi><<<grid, kGemmThreads, smem, st>>>(ta, tb, tc, p);
+      block_gemm_pair_kernel<kSbCol, kEpi>
+          <<<grid, kGemmThreads, gemm_smem_alloc<256, true, kSbCol, kEpi>(), st>>>(ta, tb, tc, p);
       break;
   }
 }
@@ -419,6 +434,7 @@ bfp8_status launch_quant(QuantParams p, bool weight, int scale_mode, cudaStream_
   if (p.C > (int64_t(1) << (glu ? 26 : 27)) || tiles >= (int64_t(1) << 31)) return BFP8_EINVAL;
   p.ctiles = static_cast<uint32_t>(p.C / 128);
   p.tiles = static_cast<uint32_t>(tiles);
+  p.stall = take_stall();
   CUtensorMap tm;
   if ((s = make_quant_tmap(&tm, p.x, p.R, glu ? 2 * p.C : p.C)) != BFP8_OK) return s;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * (glu ? 1 : 2)));
@@ -451,10 +467,19 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
     if (ws == nullptr || ws_bytes < g.ws_bytes) return BFP8_EWORKSPACE;
     if (!aligned16(ws)) return BFP8_EALIGN;
   }
+  // The fused quantised epilogue needs a whole 128-column group per thread,
+  // which the 256-column tile gives; otherwise the codes come from the
+  // split-K reduction or from the row quantiser run on C afterwards.
+  const bool fused_here = g.splits == 1 && g.bn == 256;
+  // WGRAD promotes in the column layout, except with the fused codes (the
+  // kernels' gemm_col_layout()), and its output boxes follow that layout.
+  const bool col_layout = layout == BFP8_WGRAD && !(Cq != nullptr && fused_here);
   CUtensorMap ta, tb, tc;
   if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
   if ((s = make_kmajor_tmap(&tb, B, N, K, g.pair ? g.bn / 2 : g.bn)) != BFP8_OK) return s;
-  if ((s = Cacc ? make_f32_acc_tmap(&tc, Cacc, M, N) : make_bf16_store_tmap(&tc, C, M, N)) != BFP8_OK) return s;
+  if ((s = Cacc ? make_f32_acc_tmap(&tc, Cacc, M, N, col_layout) : make_bf16_store_tmap(&tc, C, M, N, col_layout)) !=
+      BFP8_OK)
+    return s;
 
   GemmParams p;
   p.M = static_cast<int>(M);
@@ -473,13 +498,10 @@ bfp8_status gemm_impl(bfp8_layout layout, const uint8_t* A, const float* sa, con
   p.C = static_cast<uint16_t*>(C);
   p.Cacc = Cacc;
   p.Cpart = g.splits > 1 ? static_cast<float*>(ws) : nullptr;
-  // The fused quantised epilogue needs a whole 128-column group per thread,
-  // which the 256-column tile gives; otherwise the codes come from the
-  // split-K reduction or from the row quantiser run on C afterwards.
-  const bool fused_here = g.splits == 1 && g.bn == 256;
   p.Cq = fused_here ? Cq : nullptr;
   p.sCq = fused_here ? sCq : nullptr;
   p.wait_ns = dev->wait_ns;
+  p.stall = take_stall();
   const int mode = layout == BFP8_FPROP ? kSbBlock : (layout == BFP8_DGRAD ? kSbBlockT : kSbCol);
   if (g.pair) {
     s = launch_gemm_pair(mode, ta, tb, tc, p, 2 * std::min(p.units, g.slots), stream);
@@ -847,20 +869,23 @@ bfp8_status bfp8_set_wait_limit_ns(uint64_t ns) {
 }
 
 bfp8_status bfp8_set_gemm_kernel(int kind) {
-  if (kind != 0 && kind != 1) return BFP8_EINVAL;
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_gemm_kind = kind;
+  if (kind < 0 || kind > 2) return BFP8_EINVAL;
+  g_gemm_kind.store(kind, std::memory_order_relaxed);
   return BFP8_OK;
 }
 
 bfp8_status bfp8_set_gemm_splits(int splits) {
   if (splits < 0) return BFP8_EINVAL;
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_forced_splits = splits;
+  g_forced_splits.store(splits, std::memory_order_relaxed);
   return BFP8_OK;
 }
 
 uint64_t bfp8_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+bfp8_status bfp8_test_stall_next_launch(void) {
+  g_stall_next.store(1, std::memory_order_relaxed);
+  return BFP8_OK;
+}
 
 const char* bfp8_status_string(bfp8_status status) {
   switch (status) {

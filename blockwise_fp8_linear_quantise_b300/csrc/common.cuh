@@ -20,6 +20,13 @@ __device__ unsigned int g_error_site;
 
 constexpr unsigned int kErrTimeout = 1u;
 
+// Limit of the waits a kernel makes, on its way out, for its own operations
+// still in flight: TMA copies into its shared memory, and tensor-core MMAs
+// into tensor memory it is about to free.  Hardware completes those whatever
+// else has failed, so the limit is long and fixed: bfp8_set_wait_limit_ns,
+// which bounds every other wait, does not shorten it.
+constexpr uint64_t kDrainWaitNs = 5000000000ull;  // 5 s
+
 __device__ __forceinline__ void raise_error(unsigned int flag, unsigned int site) {
   if (atomicOr(&g_error_flags, flag) == 0u) atomicExch(&g_error_site, site);
 }
@@ -145,6 +152,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (.noinc: the arrival is one of the barrier's expected count).
@@ -507,6 +517,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
+      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : BFP8_R8X(0), BFP8_R8X(8), BFP8_R8X(16), BFP8_R8X(24), BFP8_R8X(32), BFP8_R8X(40), BFP8_R8X(48), BFP8_R8X(56)
+      : "r"(taddr));
+}
+
+// 16 TMEM lanes x 64 consecutive fp32 columns (16x256b shape, 8 repeats
+// along the columns): thread t receives, for repeat i, v[4i + 0..1] = lane
+// L + t/4, columns 8i + 2 (t%4) + 0..1, and v[4i + 2..3] = lane L + t/4 + 8,
+// the same columns (L = the lane field of taddr).
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : BFP8_R8(0), BFP8_R8(8), BFP8_R8(16), BFP8_R8(24)
+      : "r"(taddr));
+}
+
+// The same shape over 128 consecutive columns (16 repeats, 64 registers).
+__device__ __forceinline__ void tmem_ld16x256b_x16(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
       "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
       "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
       : BFP8_R8X(0), BFP8_R8X(8), BFP8_R8X(16), BFP8_R8X(24), BFP8_R8X(32), BFP8_R8X(40), BFP8_R8X(48), BFP8_R8X(56)

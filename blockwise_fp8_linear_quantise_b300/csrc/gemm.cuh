@@ -71,6 +71,7 @@ struct GemmParams {
   float* sCq;                   // optional [N/128, M]
   float* Cacc;                  // fp32 [M, N] accumulated into instead of C (kEpiAccum, or the split-K reduction)
   uint64_t wait_ns;
+  uint32_t stall;               // test hook: the producer first waits on a barrier nothing completes
 };
 
 // Three warpgroups: 0 and 1 promote, 2 holds the producer (warp 8) and the
@@ -94,21 +95,31 @@ static_assert(128 * kSmallRegs + 256 * kBigRegs <= kGemmThreads * kLaunchRegs, "
 // scalars of the tile's column blocks, or its BN per-column scales).
 // With kPair the CTA is one of a pair sharing a 256 x BN tile: it holds its
 // own 128 rows of A and half (BN/2 rows) of B per stage.
-template <int BN, bool kPair = false>
+// kCol: the per-column (WGRAD) promotion layout (see gemm_body): a 2 KB
+// staging area per warp, drained in passes of 32 bf16 (or 16 fp32) columns,
+// leaves room for a deeper operand ring, and sb sits in each slot in the
+// order the promotion threads read it.
+template <int BN, bool kPair = false, bool kCol = false>
 struct GemmSmem {
-  static constexpr int kStages = kPair ? 4 : (BN == 256 ? 3 : 4);
+  static constexpr int kStages = kCol ? (kPair ? 6 : (BN == 256 ? 4 : 6)) : (kPair ? 4 : (BN == 256 ? 3 : 4));
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = (kPair ? BN / 2 : BN) * 128;
   static constexpr int kAOff = 0;
   static constexpr int kBOff = kStages * kABytes;
-  static constexpr int kCWarpBytes = 32 * (BN / 2) * 2;              // one promotion warp's staging
+  static constexpr int kCWarpBytes = kCol ? 2048 : 32 * (BN / 2) * 2;  // one promotion warp's staging
   static constexpr int kCOff = kBOff + kStages * kBBytes;            // 1024-aligned
-  static constexpr int kScaleSlots = 8;                              // > kStages + 2: never the limit
-  static constexpr int kScaleSlotFloats = 128 + BN;
+  // At least kStages + 2: the producer's lead (operand ring + two TMEM
+  // buffers) never waits on a scale slot.
+  static constexpr int kScaleSlots = kCol ? kStages + 2 : 8;
+  // kCol: sb is stored as 8 runs (warp half x thread column pair) of BN/8
+  // scales, each run padded by 4 floats so that the 4 runs a warp reads at
+  // once start in different banks.
+  static constexpr int kSbStride = BN / 8 + 4;
+  static constexpr int kScaleSlotFloats = 128 + (kCol ? 8 * kSbStride : BN);
   static constexpr int kScaleOff = kCOff + 8 * kCWarpBytes;
   static constexpr int kBarOff = kScaleOff + kScaleSlots * kScaleSlotFloats * 4;
-  // barriers: full[S], empty[S], tfull[2], tempty[2], done, sfull[8], sempty[8]
-  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kScaleSlots;
+  // barriers: full[S], empty[S], tfull[2], tempty[2], done, sfull[slots], sempty[slots], stall
+  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kScaleSlots + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kTmemSlotOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -177,10 +188,198 @@ __device__ __forceinline__ void promote32(float* acc, const uint32_t (&v)[32], f
 // of 48 KB), the first CTA of the pair issues the MMAs, whose results land in
 // both CTAs' tensor memory (each CTA its own 128 rows x BN columns), and each
 // CTA promotes and stores its own rows.
+//
+// Promotion layouts.  With one scale per row (FPROP, DGRAD) each promotion
+// thread owns one tile row (TMEM lane) and BN/2 consecutive columns, read
+// with the 32x32b shape.  With the WGRAD outer product sa(i) sb(j), a thread
+// so placed needs all BN/2 column scales of every slice, and those
+// warp-uniform shared-memory reads (two wavefronts per 16 bytes) held the
+// kernel back.  The column layout (kCol) reads TMEM with the 16x256b shape
+// instead: thread t of a warp owns rows 16h + 8i + t/4 (h, i in {0, 1}) of its
+// 32 and columns 8j + 2 (t%4) + {0, 1} of its BN/2, so it needs BN/8 column
+// scales per slice, which the producer stores in that order (4 threads read 4
+// different 16-byte pieces per load).  The fused E4M3 epilogue keeps the row
+// layout (it needs whole 128-column groups per thread).
+template <int SBMODE, int kEpi>
+__host__ __device__ constexpr bool gemm_col_layout() {
+  return SBMODE == kSbCol && kEpi != kEpiCodes;
+}
+
+// Shared-memory bytes a GEMM kernel instance needs.
+template <int BN, bool kPair, int SBMODE, int kEpi>
+__host__ __device__ constexpr int gemm_smem_alloc() {
+  return GemmSmem<BN, kPair, gemm_col_layout<SBMODE, kEpi>()>::kAlloc;
+}
+
+// The promotion warps in the column layout (WGRAD), with their epilogues.
+// Warp w owns TMEM lanes 32 (w%4) .. +31 and columns (w/4) BN/2 .. +BN/2-1
+// of the CTA's tile; its thread t owns, for h, i in {0, 1}, row
+// 16h + 8i + t/4 of those 32 and, for every 8-column group j, columns
+// 8j + 2 (t%4) + {0, 1}.  acc holds them in the register order of the
+// 16x256b loads: acc[32 (h kChunks + ch) + 4 jj + 2 i + e] is row
+// 16h + 8i + t/4, column 8 (8 ch + jj) + 2 (t%4) + e.
+template <int BN, bool kPair, int kEpi, typename L>
+__device__ __forceinline__ void promote_col(const CUtensorMap& tmC, const GemmParams& p, uint8_t* smem,
+                                            const float* scales, uint64_t* tfull, uint64_t* tempty, uint64_t* sfull,
+                                            uint64_t* sempty, uint32_t tmem_base, uint32_t rank, int unit0,
+                                            int unit_step, int warp, int lane) {
+  constexpr int kCols = BN / 2;        // columns of this warp
+  constexpr int kJ = kCols / 8;        // 8-column groups of a thread
+  constexpr int kChunks = kCols / 64;  // 16x256b.x8 loads (64 columns) per 16-lane half
+  constexpr int kSlots = L::kScaleSlots, kSlotFloats = L::kScaleSlotFloats;
+  const int quad = warp & 3, half = warp >> 2;
+  const int tq = lane & 3, tr = lane >> 2;
+  uint32_t it = 0;
+  bool ok = true;
+  float acc[8 * kJ];
+  const uint32_t tempty_leader0 = kPair ? mapa_shared(&tempty[0], 0) : 0u;
+  const uint32_t tempty_leader1 = kPair ? mapa_shared(&tempty[1], 0) : 0u;
+  for (int u = unit0; u < p.units && ok; u += unit_step) {
+    UnitCoords c = unit_coords(p, u);
+    c.m0 += 128 * static_cast<int>(rank);  // this CTA's rows of a pair tile
+    const int row0 = c.m0 + quad * 32;     // first output row of this warp
+    const int col0 = c.nt * BN + half * kCols;
+#pragma unroll
+    for (int i = 0; i < 8 * kJ; ++i) acc[i] = 0.0f;
+
+    for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+      const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+      const uint32_t q = it % kSlots, qph = (it / kSlots) & 1u;
+      if (!mbar_wait(&sfull[q], qph, p.wait_ns, 0x332u) || !mbar_wait(&tfull[b], bph, p.wait_ns, 0x331u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the slice's scales of this thread's 4 rows and 2 kJ columns (the
+      // producer stored the columns in this thread's order)
+      const float* slot = scales + q * kSlotFloats;
+      float sa_r[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) sa_r[rr] = slot[quad * 32 + 16 * (rr >> 1) + 8 * (rr & 1) + tr];
+      const float4* sb4 = reinterpret_cast<const float4*>(slot + 128 + (half * 4 + tq) * L::kSbStride);
+      // 64 columns at a time (both 16-lane halves, one 16x256b.x8 load each),
+      // so that only their 16 column scales are live next to the
+      // accumulators; the buffer is handed back once its last chunk is in
+      // registers.
+      const uint32_t tbase = tmem_base + b * BN + half * kCols;
+#pragma unroll
+      for (int ch = 0; ch < kChunks; ++ch) {
+        float2 sbp[8];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float4 t = sb4[4 * ch + jj];
+          sbp[2 * jj] = make_float2(t.x, t.y);
+          sbp[2 * jj + 1] = make_float2(t.z, t.w);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          tmem_ld16x256b_x8(tbase + (static_cast<uint32_t>(quad * 32 + 16 * h) << 16) + 64 * ch, v);
+          tmem_wait_ld32(v);
+          if (h == 1 && ch + 1 == kChunks) {  // the buffer is in registers: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (kPair && rank != 0)
+                mbar_arrive_cluster(b ? tempty_leader1 : tempty_leader0);
+              else
+                mbar_arrive(&tempty[b]);
+            }
+          }
+          const uint32_t* cur = v;
+          float* a = acc + 32 * (h * kChunks + ch);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float2 sc = fmul2(make_float2(sa_r[2 * h + i], sa_r[2 * h + i]), sbp[jj]);
+              const float2 r = ffma2(make_float2(__uint_as_float(cur[4 * jj + 2 * i]), __uint_as_float(cur[4 * jj + 2 * i + 1])),
+                                     sc, make_float2(a[4 * jj + 2 * i], a[4 * jj + 2 * i + 1]));
+              a[4 * jj + 2 * i] = r.x;
+              a[4 * jj + 2 * i + 1] = r.y;
+            }
+          }
+          reg_fence32(a);
+        }
+      }
+      // the slot's scales have been read
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[q]);
+    }
+    if (!ok) break;
+
+    // ------------------------------------------------------------ epilogue
+    // acc index of row 16h + 8i + t/4, column pair (8j + 2 (t%4)) of the warp
+    auto at = [&](int h, int i, int j) -> float* { return acc + 32 * (h * kChunks + j / 8) + 4 * (j % 8) + 2 * i; };
+    if (p.splits > 1) {
+      // fp32 partial sums of this split, 8 bytes per store
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          float* prow = p.Cpart + (static_cast<int64_t>(c.split) * p.M + row0 + 16 * h + 8 * i + tr) * p.N + col0 + 2 * tq;
+#pragma unroll
+          for (int j = 0; j < kJ; ++j) {
+            const float* a = at(h, i, j);
+            *reinterpret_cast<float2*>(prow + 8 * j) = make_float2(a[0], a[1]);
+          }
+        }
+    } else {
+      // Through this warp's 2 KB staging area (rows of 64 bytes, 64-byte
+      // swizzle: 16-byte chunk k of row r at chunk k ^ ((r >> 1) & 3)), one
+      // TMA box of 32 rows per pass: 32 bf16 columns (plain) or 16 fp32
+      // columns added into the output (accumulate).
+      constexpr bool kAcc = kEpi == kEpiAccum;
+      constexpr int kPassCols = kAcc ? 16 : 32;
+      uint8_t* stg = smem + L::kCOff + warp * L::kCWarpBytes;
+#pragma unroll
+      for (int ps = 0; ps < kCols / kPassCols; ++ps) {
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous pass's box has been read
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t r = 16 * h + 8 * i + tr, sw = (r >> 1) & 3u;
+#pragma unroll
+            for (int g = 0; g < kPassCols / 8; ++g) {  // 8-column group g of the pass
+              const float* a = at(h, i, ps * (kPassCols / 8) + g);
+              if constexpr (kAcc) {
+                // columns 8g' + 2tq, +1: byte 4 (8g' + 2tq) = chunk 2g' + tq/2,
+                // offset 8 (tq%2).  Lanes 8..15 and 24..31 (rows with bit 1
+                // set) store the other group g' = g ^ 1 first, which puts the
+                // 4 rows of each 16-lane phase in different banks.
+                const float* o = at(h, i, ps * (kPassCols / 8) + (g ^ 1));
+                const bool flip = (lane >> 3) & 1;
+                const float2 val = flip ? make_float2(o[0], o[1]) : make_float2(a[0], a[1]);
+                const uint32_t chunk = static_cast<uint32_t>(2 * (g ^ static_cast<int>(flip)) + (tq >> 1));
+                *reinterpret_cast<float2*>(stg + r * 64 + ((chunk ^ sw) << 4) + 8 * (tq & 1)) = val;
+              } else {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(a[0], a[1]);
+                *reinterpret_cast<uint32_t*>(stg + r * 64 + ((static_cast<uint32_t>(g) ^ sw) << 4) + 4 * tq) =
+                    *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            }
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kAcc)
+            tma_reduce_add_2d(&tmC, stg, col0 + kPassCols * ps, row0);
+          else
+            tma_store_2d(&tmC, stg, col0 + kPassCols * ps, row0);
+          bulk_commit_group();
+        }
+      }
+    }
+  }
+}
+
 template <int BN, int SBMODE, bool kPair, int kEpi>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                                           const GemmParams& p) {
-  using L = GemmSmem<BN, kPair>;
+  constexpr bool kCol = gemm_col_layout<SBMODE, kEpi>();
+  using L = GemmSmem<BN, kPair, kCol>;
   constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -192,6 +391,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint64_t* done = bars + 2 * kStages + 4;
   uint64_t* sfull = bars + 2 * kStages + 5;  // scale slot landed (32 producer lanes)
   uint64_t* sempty = sfull + L::kScaleSlots;  // scale slot read (8 promotion warps)
+  uint64_t* stall = sempty + L::kScaleSlots;  // never completed (test hook p.stall)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
   float* scales = reinterpret_cast<float*>(smem + L::kScaleOff);
   constexpr int kSlots = L::kScaleSlots, kSlotFloats = L::kScaleSlotFloats;
@@ -211,6 +411,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_init(&tempty[b], kPair ? 16 : 8);  // one arrival per promotion warp (of both CTAs)
     }
     mbar_init(done, 1);
+    mbar_init(stall, 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sfull[i], 32);
       mbar_init(&sempty[i], 8);
@@ -249,6 +450,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const int nkb = p.K / 128;
     uint32_t it = 0;
     bool ok = true;
+    // Test hook: a wait that nothing satisfies, so that it expires after the
+    // wait limit and the kernel takes its early-exit path before any copy.
+    if (p.stall != 0u) ok = mbar_wait(stall, 0, p.wait_ns, 0x300u);
     for (int u = unit0; u < p.units && ok; u += unit_step) {
       UnitCoords c = unit_coords(p, u);
       const int m_rows = c.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
@@ -264,7 +468,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         float* slot = scales + q * kSlotFloats;
         cp_async16(slot + 4 * lane, p.sa + static_cast<int64_t>(kb) * p.M + m_rows + 4 * lane);
-        if constexpr (SBMODE == kSbCol) {
+        if constexpr (kCol) {
+          // columns (col, col + 1) of the tile, col = 2 (32 r + lane), go to
+          // the run of warp half col / (BN/2) and thread column pair
+          // (col % 8) / 2, at position 2 (col % (BN/2)) / 8 of the run
+          constexpr int kHalfCols = BN / 2;
+#pragma unroll
+          for (int r = 0; r < BN / 64; ++r) {
+            const int col = 2 * (32 * r + lane);
+            const int cc = col % kHalfCols;
+            const int dst = ((col / kHalfCols) * 4 + (cc % 8) / 2) * L::kSbStride + 2 * (cc / 8);
+            cp_async8(slot + 128 + dst, p.sb + static_cast<int64_t>(kb) * p.N + c.nt * BN + col);
+          }
+        } else if constexpr (SBMODE == kSbCol) {
 #pragma unroll
           for (int r = 0; r < BN / 128; ++r)
             cp_async16(slot + 128 + 128 * r + 4 * lane,
@@ -304,7 +520,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     if (lane == 0 && (!kPair || rank == 0)) {
       for (uint32_t j = 0; j < kStages && j < it; ++j) {
         const uint32_t f = it - 1 - j;
-        mbar_wait(&full[f % kStages], (f / kStages) & 1u, p.wait_ns, 0x302u);
+        mbar_wait(&full[f % kStages], (f / kStages) & 1u, kDrainWaitNs, 0x302u);
       }
     }
     } else if (warp == kMmaWarp) {
@@ -347,11 +563,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       } else {
         mma_commit(done);
       }
-      mbar_wait(done, 0, p.wait_ns, 0x313u);
+      mbar_wait(done, 0, kDrainWaitNs, 0x313u);
     }
     }
   } else {
     setmaxnreg_inc<kBigRegs>();
+    if constexpr (kCol) {
+      promote_col<BN, kPair, kEpi, L>(tmC, p, smem, scales, tfull, tempty, sfull, sempty, tmem_base, rank, unit0,
+                                      unit_step, warp, lane);
+    } else {
     // ------------------------------------------------------------ promotion
     constexpr int kCols = BN / 2;  // output columns per promotion thread
     const int quad = warp & 3, half = warp >> 2;
@@ -516,6 +736,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         for (int i = 0; i < kCols / 4; ++i)
           *reinterpret_cast<float4*>(prow + 4 * i) = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
       }
+    }
     }
   }
 

@@ -58,6 +58,7 @@ struct QuantParams {
   uint64_t wait_ns;
   uint32_t ctiles, tiles;  // C/128 and (R/128)(C/128), filled in by the launcher
   uint16_t* h;             // prologue only: bf16 [R, C] copy of h, or null
+  uint32_t stall;          // test hook: warp 0 first waits on a barrier nothing completes
 };
 
 // Which outputs a kernel instance writes (a template bit set).
@@ -70,13 +71,13 @@ constexpr int kQStages = 3;
 constexpr int kQTileBytes = 128 * 256;  // bf16 tile
 
 // Shared memory: the ring (one tile per slot, or the g and u tiles of the
-// SiLU-gated prologue), then full[3], empty[3], redbar[2] and float[2][8]
-// (weight block amax), plus room to align the base to 1024.
+// SiLU-gated prologue), then full[3], empty[3], redbar[2], stall and
+// float[2][8] (weight block amax), plus room to align the base to 1024.
 template <bool kGlu>
 struct QuantLayout {
   static constexpr int kSlot = (kGlu ? 2 : 1) * kQTileBytes;
   static constexpr int kBarOff = kQStages * kSlot;
-  static constexpr int kRedOff = kBarOff + (2 * kQStages + 2) * 8;
+  static constexpr int kRedOff = kBarOff + (2 * kQStages + 3) * 8;
   static constexpr int kSmemBytes = kRedOff + 2 * kQComputeWarps * 4 + 1024;
 };
 constexpr int kQuantSmemBytes = QuantLayout<false>::kSmemBytes;
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + kQStages;
   uint64_t* redbar = empty + kQStages;  // weight block amax / prologue h exchange, by tile parity
+  uint64_t* stall = redbar + 2;         // never completed (test hook p.stall)
   float* red = reinterpret_cast<float*>(smem + L::kRedOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
     }
     mbar_init(&redbar[0], kGlu ? kQuantThreads : kQComputeWarps);
     mbar_init(&redbar[1], kGlu ? kQuantThreads : kQComputeWarps);
+    mbar_init(stall, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -244,7 +247,11 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
   // iteration j) tile j-1+kQStages into the slot tile j-1 used.
   TileWalk fill = cur;
   uint32_t issued = 0;  // tiles of this CTA issued so far (warp 0)
-  if (warp == 0) {
+  // Test hook: a wait that nothing satisfies, so that it expires after the
+  // wait limit; warp 0 then issues no copy and every warp's first wait on a
+  // tile expires too, so the kernel ends with nothing in flight.
+  const bool stalled = p.stall != 0u && warp == 0 && !mbar_wait(stall, 0, p.wait_ns, kWeight ? 0x200u : 0x100u);
+  if (warp == 0 && !stalled) {
     for (; issued < kQStages && fill.t < tiles; ++issued) {
       quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + issued * L::kSlot, &full[issued], lane);
       fill.advance(step, drt, dct, ctiles);
@@ -431,7 +438,7 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
   // exit j counts all tiles of the CTA and nothing is waited for.
   if (warp == 0 && lane == 0) {
     for (uint32_t k = j; k < issued; ++k)
-      mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, p.wait_ns, kWeight ? 0x212u : 0x112u);
+      mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, kDrainWaitNs, kWeight ? 0x212u : 0x112u);
   }
 }
 

@@ -298,7 +298,8 @@ def set_wait_limit_ns(ns):
 
 
 def set_gemm_kernel(kind):
-    """0: CTA-pair 256x256 tiles where the shape allows (default); 1: single-CTA tiles only."""
+    """0: CTA-pair 256x256 tiles for FPROP/DGRAD where the shape allows (default); 1: single-CTA tiles only;
+    2: CTA pairs for WGRAD as well."""
     _check(_lib.load().bfp8_set_gemm_kernel(int(kind)), "set_gemm_kernel")
 
 
@@ -309,3 +310,9 @@ def set_gemm_splits(splits):
 def launch_count():
     """Kernels the library has launched in this process so far."""
     return int(_lib.load().bfp8_launch_count())
+
+
+def test_stall_next_launch():
+    """Test hook: the next quantiser or GEMM launch makes one bounded wait that nothing satisfies (it expires
+    after the wait limit, and sync_status() then reports BFP8_ETIMEOUT)."""
+    _check(_lib.load().bfp8_test_stall_next_launch(), "test_stall_next_launch")

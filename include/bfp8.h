@@ -19,9 +19,14 @@
  *   - All matrices are row-major and contiguous.  "bf16" is IEEE bfloat16.
  *   - Every dimension must be a positive multiple of 128 (BFP8_EINVAL).
  *   - Every device pointer must be 16-byte aligned (BFP8_EALIGN).
- *   - The caller owns all memory.  The library allocates no device memory
- *     and keeps no state between calls except a per-device error word and
- *     cached device attributes.
+ *   - The caller owns all memory.  The library allocates no device memory.
+ *     What it keeps between calls is a per-device error word, per-device
+ *     set-up done on first use (kernel attributes, device queries, the
+ *     device address of the static scratch array below) and that array:
+ *     BFP8_NOALLOC_SCRATCH_BYTES of device memory in the loaded module,
+ *     used only by bfp8_fp8_block_gemm_noalloc, whose contents persist
+ *     between its calls.  The set-up does not survive cudaDeviceReset():
+ *     do not call the library on a device after resetting it.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream).  The return value reports argument and
  *     launch errors only; bfp8_sync_status() reports errors raised on the
@@ -210,22 +215,27 @@ bfp8_status bfp8_fp8_block_gemm_accumulate(bfp8_layout layout,
 
 /*
  * The same GEMM as bfp8_fp8_block_gemm, for callers that cannot allocate
- * device memory: code that runs where cudaMalloc is not allowed or not
- * wanted (inside a host callback, a custom allocator, a real-time loop
- * that must not synchronise the device), or that has no way to hand over a
- * workspace.  The paper has no counterpart; this is a convenience of the
- * library.
+ * device memory for its split-K workspace and have none to hand over: a
+ * process whose device memory is all reserved by another framework's memory
+ * pool, where a cudaMalloc would fail; a latency-bound loop where cudaMalloc
+ * and cudaFree, which may synchronise the device, must not run; code bound to
+ * an interface that has no workspace argument.  The paper has no counterpart;
+ * this is a convenience of the library.  Call it from ordinary host code, as
+ * every other entry point: it makes CUDA runtime calls (device queries,
+ * kernel launches).
  *
  * Arguments, layouts and results are those of bfp8_fp8_block_gemm without
  * the workspace: the caller still passes every input and output.  The
  * split-K partial sums go to one static device array of
  * BFP8_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
  * loads the library holds until the process exits.  This entry point calls
- * no cudaMalloc, cudaFree or other allocating routine.
+ * no cudaMalloc, cudaFree or other allocating routine.  Its results equal
+ * bfp8_fp8_block_gemm's bit for bit (the same plan runs the same kernels).
  *
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *     first call before any stream capture on the device.  The kept address
+ *     does not survive cudaDeviceReset() (see the conventions above).
  *   - Every call shares the one array.  Calls that run at the same time on
  *     the GPU (different streams or threads) race on it and corrupt each
  *     other's results: serialise them.  Each call overwrites every partial
@@ -342,19 +352,37 @@ bfp8_status bfp8_linear_bwd_main_grad(const void* dY,
 bfp8_status bfp8_sync_status(bfp8_stream_t stream);
 
 /*
- * Sets the limit, in nanoseconds, of every device-side wait the kernels make
- * on the current device from now on (default 2e9).  Used by tests to make a
- * wait expire on purpose; 0 restores the default.
+ * Sets the limit, in nanoseconds, of the device-side waits the kernels make
+ * on the current device from now on (default 2e9); 0 restores the default.
+ * Not affected: the waits a kernel makes on its way out for its own TMA
+ * copies and MMAs still in flight, which have a fixed 5 s limit, so that a
+ * kernel that gave up never leaves a copy into its shared memory or an MMA
+ * into tensor memory it frees.  The tests shorten the limit and make a wait
+ * expire on purpose (bfp8_test_stall_next_launch), then check that
+ * bfp8_sync_status reports BFP8_ETIMEOUT and that the next call with the
+ * default limit is exact.
  */
 bfp8_status bfp8_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook of the timeout path (there is no counterpart in the paper).  The
+ * next quantiser or GEMM kernel this library launches, on any device, first
+ * makes one device-side wait on a barrier that nothing completes.  The wait
+ * gives up after the current wait limit (bfp8_set_wait_limit_ns), the kernel
+ * leaves early without starting any copy or MMA, and bfp8_sync_status reports
+ * BFP8_ETIMEOUT; that call's outputs are undefined.  Later launches are
+ * unaffected.  The hook only ever delays a kernel by the wait limit: it never
+ * faults, traps or hangs the GPU.  Always returns BFP8_OK.
+ */
+bfp8_status bfp8_test_stall_next_launch(void);
 
 /*
  * Selects the GEMM tiling for every later call in the process: 0 (default)
  * uses 256 x 256 output tiles computed by pairs of CTAs (tensor-core pair
  * MMAs) for FPROP and DGRAD whenever both output dimensions are multiples of
  * 256, and 128 x 256 (or 128 x 128) single-CTA tiles otherwise (always for
- * WGRAD); 1 always uses single-CTA tiles.
- * Both give results within the same tolerance of the oracle.
+ * WGRAD); 1 always uses single-CTA tiles; 2 uses CTA pairs for WGRAD as well.
+ * All give results within the same tolerance of the oracle.
  * Errors: EINVAL for any other value.
  */
 bfp8_status bfp8_set_gemm_kernel(int kind);

@@ -131,7 +131,7 @@ def gemm_smem(pair, bn):
     slots, slot_floats = 8, 128 + bn
     scale_off = c_off + 8 * c_warp
     bar_off = scale_off + slots * slot_floats * 4
-    bars = 2 * stages + 5 + 2 * slots
+    bars = 2 * stages + 5 + 2 * slots + 1  # full, empty, tfull[2], tempty[2], done, sfull, sempty, stall
     tmem_slot = bar_off + bars * 8
     return dict(stages=stages, a_bytes=a_bytes, b_bytes=b_bytes, b_off=b_off, c_off=c_off, c_warp=c_warp,
                 scale_off=scale_off, slot_bytes=slot_floats * 4, bar_off=bar_off, tmem_slot=tmem_slot,

@@ -71,10 +71,10 @@ def rand_layer(M, N, K, seed):
     return np32(X), np32(W), np32(dY)
 
 
-@pytest.fixture(params=[0, 1], ids=["pair-tiles", "single-cta-tiles"])
+@pytest.fixture(params=[0, 1, 2], ids=["pair-tiles", "single-cta-tiles", "pair-tiles-wgrad"])
 def gemm_kind(request):
-    """Run a test with the CTA-pair GEMM (where the shape allows) and with
-    single-CTA tiles only."""
+    """Run a test with the CTA-pair GEMM (where the shape allows), with
+    single-CTA tiles only, and with CTA pairs for WGRAD as well."""
     ops.set_gemm_kernel(request.param)
     yield request.param
     ops.set_gemm_kernel(0)
