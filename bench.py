@@ -112,8 +112,8 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=28, help="stack28 only: layers to run (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=512)
-    ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--ref-sample-tokens", type=int, default=1024)
     ap.add_argument("--scale-mode", choices=["amax448", "pow2", "mul_recip"], default="amax448",
                     help="group scale rule: amax/448 with codes of x/s (default), the power-of-two mode, or "
                          "amax/448 with codes of x * fp32(448/amax)")
@@ -173,12 +173,28 @@ def sum_over_ranks(x, group):
 
 
 def load_peaks():
+    """(peaks, basis): the measured denominators, with 'sustained_sm_mhz', the
+    median SM clock under load while the sustained bf16 peak was measured
+    (None when the file does not record it)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
-    return dict(FALLBACK_PEAKS), "fallback"
+        out = {k: float(d[k]) for k in FALLBACK_PEAKS}
+        out["sustained_sm_mhz"] = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
+        return out, "measured"
+    out = dict(FALLBACK_PEAKS)
+    out["sustained_sm_mhz"] = None
+    return out, "fallback"
+
+
+def clock_normalised(achieved, peak, peak_mhz, run_mhz):
+    """achieved / (peak scaled from the clock it was measured at to the run's
+    median SM clock): a tensor-bound rate scales with the SM clock, so this
+    compares the kernel and the peak at the same clock."""
+    if not peak_mhz or not run_mhz:
+        return None
+    return round(achieved / (peak * run_mhz / peak_mhz), 4)
 
 
 def linear_list(wl, layers):
@@ -268,13 +284,21 @@ class ClockSampler:
         return summarise_clocks(rows)
 
 
-def cpu_threads():
+def cpu_model():
+    """The host CPU's model name (Linux /proc/cpuinfo), or None."""
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info()]
-        return max(n) if n else 1
-    except Exception:
-        return 1
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def host_info():
+    from oracle import parallel
+    return {"nproc": os.cpu_count(), "usable_cpus": parallel.workers(), "cpu_model": cpu_model()}
 
 
 # ------------------------------------------------------------ oracle timing
@@ -300,16 +324,24 @@ def oracle_sample(wl, specs, tokens):
 
 
 def run_oracle(sample, scale_mode="amax448"):
-    """Oracle linear forward (+ backward) over the sample; returns GEMM FLOPs."""
-    from oracle import gemm as ogemm
+    """Oracle linear forward (+ backward) over the sample, its GEMMs spread
+    over every host core by blocks of output rows (bit-identical to the
+    serial oracle); returns GEMM FLOPs."""
+    from oracle import parallel
     flops = 0
     for x, w, dy in sample:
-        _, saved = ogemm.linear_fwd(x, w, scale_mode=scale_mode)
+        _, saved = parallel.linear_fwd(x, w, scale_mode=scale_mode)
         flops += 2 * x.shape[0] * w.shape[0] * x.shape[1]
         if dy is not None:
-            ogemm.linear_bwd(dy, saved, scale_mode=scale_mode)
+            parallel.linear_bwd(dy, saved, scale_mode=scale_mode)
             flops += 4 * x.shape[0] * w.shape[0] * x.shape[1]
     return flops
+
+
+def oracle_cores():
+    from oracle import parallel
+    parallel.pool()  # started (spawn) before the timing
+    return parallel.workers()
 
 
 def describe_sample(sample):
@@ -325,6 +357,7 @@ def reference_arm(args):
     wl = workloads.make(args.workload)
     specs = linear_list(wl, args.layers)
     sample = oracle_sample(wl, specs, args.ref_sample_tokens)
+    cores = oracle_cores()
     for _ in range(args.warmup):
         run_oracle(sample, args.scale_mode)
     t0 = time.perf_counter()
@@ -333,13 +366,14 @@ def reference_arm(args):
         flops += run_oracle(sample, args.scale_mode)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    cores = cpu_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
             "data": "synthetic", "config": workload_config(wl, specs, args.layers, args.scale_mode),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "per step: " + describe_sample(sample)},
+                             "sample": "per step: " + describe_sample(sample)
+                                       + " (GEMMs by output-row blocks over a spawn process pool)",
+                             **host_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -681,12 +715,18 @@ def gpu_arm(args):
                 "frac": round(g_achieved / fp8_sust, 4),
                 "peak_basis": f"{FP8_PER_BF16:g} x {basis} bf16 sustained ({peaks['bf16_tflops_sustained']}) TFLOP/s",
                 "frac_of_burst": round(g_achieved / fp8_burst, 4),
+                "frac_clock_normalised": clock_normalised(g_achieved, fp8_sust, peaks["sustained_sm_mhz"],
+                                                          clk.get("sm_mhz")),
+                "clock_basis": f"sustained peak measured at a median {peaks['sustained_sm_mhz']} MHz, scaled to this "
+                               f"run's median {clk.get('sm_mhz')} MHz",
                 "traffic": traffic, "flops_per_call": round(g_flops / max(g_calls, 1))}
     roofline_q = None
     if q_achieved is not None:
         roofline_q = {"bound": "hbm", "kernel": "quantize_tile_kernel (activation dual + weight)",
                       "achieved": round(q_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": round(q_achieved / peaks["hbm_gbs"], 4), "peak_basis": f"{basis} HBM copy",
+                      "frac_clock_normalised": round(q_achieved / peaks["hbm_gbs"], 4),
+                      "clock_basis": "HBM bandwidth does not scale with the SM clock: the same as frac",
                       "bytes_per_call": round(q_bytes / max(sum(x[0] for x in q), 1)), "traffic": rec.get("quant")}
 
     # e2e through the public fused calls with host buffers
@@ -723,11 +763,14 @@ def gpu_arm(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = oracle_sample(wl, specs, args.cpu_sample_tokens)
+        cores = oracle_cores()
         t0 = time.perf_counter()
         f = run_oracle(sample, args.scale_mode)
         dt = time.perf_counter() - t0
-        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-               "sample": describe_sample(sample) + f" ({dt:.1f} s)", "host_cpus": os.cpu_count()}
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": describe_sample(sample) + f" ({dt:.1f} s; GEMMs by output-row blocks over a spawn "
+                                                   f"process pool of {cores})",
+               **host_info()}
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
