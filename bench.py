@@ -372,7 +372,7 @@ def reference_arm(args):
             "data": "synthetic", "config": workload_config(wl, specs, args.layers, args.scale_mode),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "per step: " + describe_sample(sample)
-                                       + " (GEMMs by output-row blocks over a spawn process pool)",
+                                       + " (quantisers and GEMMs split over a spawn process pool)",
                              **host_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -768,7 +768,7 @@ def gpu_arm(args):
         f = run_oracle(sample, args.scale_mode)
         dt = time.perf_counter() - t0
         cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": describe_sample(sample) + f" ({dt:.1f} s; GEMMs by output-row blocks over a spawn "
+               "sample": describe_sample(sample) + f" ({dt:.1f} s; quantisers and GEMMs split over a spawn "
                                                    f"process pool of {cores})",
                **host_info()}
 

@@ -287,3 +287,39 @@ def test_unknown_scale_mode_is_rejected():
     for bad in (3, 7, -1):
         assert _lib.load().bfp8_quantize_act_1x128_ex(x.data_ptr(), 128, 128, q.data_ptr(), s.data_ptr(), None,
                                                       None, bad, st) == 1
+
+
+def test_weight_block_worked_example_on_gpu():
+    """The hand-worked 256 x 256 weight fixture: block scales and the listed
+    codes, in both the fprop (Wq) and dgrad (WqT) layouts."""
+    from test_oracle_quant import golden_weight_block
+    w, scales, codes = golden_weight_block()
+    q, qT, s = ops.quantize_w_128x128(to_gpu(w, torch.bfloat16))
+    assert ops.sync_status() == 0
+    s = s.cpu().numpy()
+    for (bi, bj), bits in scales.items():
+        assert s[bi, bj].view(np.uint32) == bits, (bi, bj)
+    qn, qTn = u8(q), u8(qT)
+    for (ii, jj), (_, code) in codes.items():
+        assert qn[ii, jj] == code and qTn[jj, ii] == code, (ii, jj)
+    check_w(torch.from_numpy(w).to(torch.bfloat16))
+
+
+def test_stack_weights_all_layers():
+    """Every weight of the 28-layer stack (QKV, O, gate+up, down per layer),
+    as the benchmark's step quantises them, bit-exact against the oracle (run
+    over the host's cores; it changes no bit)."""
+    from oracle import parallel
+    wl = workloads.make("stack28")
+    try:
+        for layer in range(28):
+            for tag in ("w_qkv", "w_o", "w_gu", "w_down"):
+                w = workloads.tensor(wl, tag, layer)
+                q, qT, s = ops.quantize_w_128x128(w.to(dev()))
+                assert ops.sync_status() == 0
+                oq, oqT, os_ = parallel.quantize_w_128x128(np32(w))
+                assert_codes_equal(u8(q), oq, f"Wq {tag} layer {layer}")
+                assert_codes_equal(u8(qT), oqT, f"WqT {tag} layer {layer}")
+                assert_scales_equal(s.cpu().numpy(), os_, f"sW {tag} layer {layer}")
+    finally:
+        parallel.shutdown()

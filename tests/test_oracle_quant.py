@@ -380,3 +380,30 @@ def test_mul_recip_invariants_rows_tokens_weights(name, tag):
     mb = quant.group_multiplier(blk)
     ref = quant.quantize_values_mul(x.reshape(R // 128, 128, C // 128, 128), mb[:, None, :, None]).reshape(R, C)
     assert np.array_equal(wq, ref)
+
+
+def golden_weight_block():
+    """W [256, 256] of the hand-worked weight fixture, and its listed scales
+    and codes."""
+    i, j = np.meshgrid(np.arange(256), np.arange(256), indexing="ij")
+    w = ((((7 * i + 3 * j) % 17) - 8) * 2.0 ** -8).astype(np.float32)
+    w[5, 7], w[0, 128], w[255, 127], w[128, 255] = 448.0, -3.5, 0.875, 1.0
+    scales, codes = {}, {}
+    for row in read_golden("weight_block_worked_example.txt"):
+        if row[0] == "scale":
+            scales[(int(row[1]), int(row[2]))] = int(row[4], 16)
+        else:
+            codes[(int(row[1]), int(row[2]))] = (np.float32(float(row[3])), int(row[5], 16))
+    return w, scales, codes
+
+
+def test_weight_block_worked_example():
+    w, scales, codes = golden_weight_block()
+    assert np.array_equal(bf16_exact(w).view(np.uint32), w.view(np.uint32))
+    q, qT, s = quant.quantize_w_128x128(w)
+    assert s.shape == (2, 2)
+    for (bi, bj), bits in scales.items():
+        assert s[bi, bj].view(np.uint32) == bits, (bi, bj)
+    for (ii, jj), (x, code) in codes.items():
+        assert w[ii, jj] == x
+        assert q[ii, jj] == code and qT[jj, ii] == code, (ii, jj)
