@@ -127,6 +127,9 @@ def parse_args(argv=None):
                     help="time the SiLU-gated prologue (bfp8_swiglu_quantize_1x128) on the down projection's input")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
+    ap.add_argument("--probe-mx", action="store_true",
+                    help="compare the MXFP8 1x32 recipe with the blockwise one on the mlp_down layer: accuracy of "
+                         "every GEMM against the unquantised product, and time of quantisers and GEMMs")
     return ap.parse_args(argv)
 
 
@@ -834,6 +837,67 @@ def fp8_peak_probe():
     return 0
 
 
+def mx_probe(args):
+    """The MXFP8 1x32 recipe against the blockwise 1x128 / 128x128 recipe on
+    the mlp_down layer (X [8192, 6144], W [2048, 6144], dY [8192, 2048]):
+    for FPROP, DGRAD and WGRAD, the relative Frobenius error of each recipe's
+    bf16 output against the unquantised bf16 operands' product (fp64 on the
+    GPU, a measurement reference only), and the median time of each recipe's
+    quantisers and GEMMs over 10 calls after 3 warm-up calls."""
+    import torch
+    from blockwise_fp8_linear_quantise_b300 import ops, workloads
+    wl = workloads.make("mlp_down")
+    X, W, dY = (workloads.tensor(wl, t).to("cuda") for t in ("x", "w", "dy"))
+    M, K = X.shape
+    N = W.shape[0]
+
+    def med_ms(fn, n=10):
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return statistics.median(times)
+
+    exact = {"fprop": X.double() @ W.double().t(), "dgrad": dY.double() @ W.double(),
+             "wgrad": dY.double().t() @ X.double()}
+    rel = lambda got, want: float(torch.linalg.norm(got.double() - want) / torch.linalg.norm(want))
+    # blockwise recipe
+    bq = {}
+    q_block = lambda: (ops.quantize_act_1x128(X, rows=True, tokens=True), ops.quantize_w_128x128(W),
+                       ops.quantize_act_1x128(dY, rows=True, tokens=True))
+    (Xq, sX, XqT, sXT), (Wq, WqT, sW), (dYq, sdY, dYqT, sdYT) = q_block()
+    bgemm = {"fprop": lambda: ops.fp8_block_gemm(ops.FPROP, Xq, sX, Wq, sW),
+             "dgrad": lambda: ops.fp8_block_gemm(ops.DGRAD, dYq, sdY, WqT, sW),
+             "wgrad": lambda: ops.fp8_block_gemm(ops.WGRAD, dYqT, sdYT, XqT, sXT)}
+    # MXFP8 1x32 recipe
+    q_mx = lambda: (ops.quantize_mx_1x32(X, rows=True, tokens=True), ops.quantize_mx_1x32(W, rows=True, tokens=True),
+                    ops.quantize_mx_1x32(dY, rows=True, tokens=True))
+    (mXq, msX, mXqT, msXT), (mWq, msW, mWqT, msWT), (mdYq, msdY, mdYqT, msdYT) = q_mx()
+    mgemm = {"fprop": lambda: ops.mx_gemm(mXq, msX, mWq, msW), "dgrad": lambda: ops.mx_gemm(mdYq, msdY, mWqT, msWT),
+             "wgrad": lambda: ops.mx_gemm(mdYqT, msdYT, mXqT, msXT)}
+    out = {"probe": "mxfp8_1x32_vs_blockwise", "workload": f"mlp_down X [{M}, {K}], W [{N}, {K}], dY [{M}, {N}]",
+           "quantise_ms": {"blockwise": round(med_ms(q_block), 4), "mx_1x32": round(med_ms(q_mx), 4)},
+           "gemm": {}}
+    for name in ("fprop", "dgrad", "wgrad"):
+        Mg, Ng = exact[name].shape
+        Kg = K if name == "fprop" else (N if name == "dgrad" else M)
+        flop = 2.0 * Mg * Ng * Kg
+        tb, tm = med_ms(bgemm[name]), med_ms(mgemm[name])
+        out["gemm"][name] = {"rel_fro_err_vs_unquantised": {"blockwise": rel(bgemm[name](), exact[name]),
+                                                             "mx_1x32": rel(mgemm[name](), exact[name])},
+                             "TFLOP/s": {"blockwise": round(flop / (tb * 1e-3) / 1e12, 1),
+                                         "mx_1x32": round(flop / (tm * 1e-3) / 1e12, 1)}}
+    assert ops.sync_status() == 0
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def swiglu_probe(args):
     """The SiLU-gated prologue on the down projection's input, gate+up output
     gu [8192, 12288] drawn as the mlp_down recipe (G, U ~ 0.5 t(4)): both
@@ -884,6 +948,8 @@ def main(argv=None):
         return fp8_peak_probe()
     if args.probe_swiglu:
         return swiglu_probe(args)
+    if args.probe_mx:
+        return mx_probe(args)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

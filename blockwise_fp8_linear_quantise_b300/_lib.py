@@ -18,6 +18,8 @@ SIGNATURES = {
     "bfp8_quantize_act_1x128_ex": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_int, c_p]),
     "bfp8_quantize_w_128x128_ex": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_int, c_p]),
     "bfp8_swiglu_quantize_1x128": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_int, c_p]),
+    "bfp8_quantize_mx_1x32": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p]),
+    "bfp8_mx_gemm": (c_int, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p]),
     "bfp8_fp8_block_gemm": (c_int, [c_int, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "bfp8_gemm_workspace_bytes": (c_sz, [c_int, c_i64, c_i64, c_i64]),
     "bfp8_fp8_block_gemm_accumulate": (c_int, [c_int, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p, c_sz, c_p]),

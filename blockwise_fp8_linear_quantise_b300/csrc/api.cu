@@ -17,6 +17,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "quant.cuh"
+#include "gemm_mx.cuh"
 
 namespace {
 
@@ -91,6 +92,11 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_SET_QUANT_SMEM_ALL(kScaleAmax448)
     BFP8_SET_QUANT_SMEM_ALL(kScalePow2)
     BFP8_SET_QUANT_SMEM_ALL(kScaleMulRecip)
+    BFP8_SET_QUANT_SMEM(false, kQRows, kScaleMx32)
+    BFP8_SET_QUANT_SMEM(false, kQCols, kScaleMx32)
+    BFP8_SET_QUANT_SMEM(false, kQRows | kQCols, kScaleMx32)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxSmem::kAlloc);
 #undef BFP8_SET_QUANT_SMEM_ALL
     // the SiLU-gated prologue: one CTA per SM with two tiles per ring slot
 #define BFP8_SET_GLU_SMEM_ALL(SCALE)                                                      \
@@ -180,6 +186,11 @@ bfp8_status device_state(DeviceState** out) {
     BFP8_CHECK_PAIR_REGS(kSbBlock, kEpiAccum)
     BFP8_CHECK_PAIR_REGS(kSbBlockT, kEpiAccum)
     BFP8_CHECK_PAIR_REGS(kSbCol, kEpiAccum)
+    {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, mx_gemm_kernel) != cudaSuccess) return BFP8_ECUDA;
+      if (fa.numRegs != kLaunchRegs) return BFP8_EUNSUPPORTED;
+    }
 #undef BFP8_CHECK_PAIR_REGS
     // How many CTA pairs can be resident at once (the persistent pair grid).
     {
@@ -419,6 +430,10 @@ bfp8_status launch_quant_scale(const CUtensorMap& tm, const QuantParams& p, unsi
                                cudaStream_t st) {
   if (scale_mode == kScalePow2) return launch_quant_mode<kWeight, kScalePow2, kGlu>(tm, p, grid, st);
   if (scale_mode == kScaleMulRecip) return launch_quant_mode<kWeight, kScaleMulRecip, kGlu>(tm, p, grid, st);
+  if constexpr (!kWeight && !kGlu) {
+    if (scale_mode == kScaleMx32) return launch_quant_mode<false, kScaleMx32, false>(tm, p, grid, st);
+  }
+  if (scale_mode == kScaleMx32) return BFP8_EINVAL;
   return launch_quant_mode<kWeight, kScaleAmax448, kGlu>(tm, p, grid, st);
 }
 
@@ -443,6 +458,7 @@ bfp8_status launch_quant(QuantParams p, bool weight, int scale_mode, cudaStream_
   else
     s = weight ? launch_quant_scale<true, false>(tm, p, grid, scale_mode, st)
                : launch_quant_scale<false, false>(tm, p, grid, scale_mode, st);
+  if (s != BFP8_OK) return s;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cuda_status(cudaGetLastError());
 }
@@ -731,6 +747,55 @@ bfp8_status bfp8_fp8_block_gemm_accumulate(bfp8_layout layout, const uint8_t* A,
   if (C_f32 == nullptr) return BFP8_EINVAL;
   return gemm_impl(layout, A, sa, B, sb, M, N, K, nullptr, nullptr, nullptr, ws, ws_bytes,
                    reinterpret_cast<cudaStream_t>(stream), C_f32);
+}
+
+bfp8_status bfp8_quantize_mx_1x32(const void* x, int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                  bfp8_stream_t stream) {
+  if (!x || (!q && !qT) || (q && !s) || (qT && !sT)) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(K)) return BFP8_EINVAL;
+  if (!aligned16(x) || (q && (!aligned16(q) || !aligned16(s))) || (qT && (!aligned16(qT) || !aligned16(sT))))
+    return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status st = device_state(&dev);
+  if (st != BFP8_OK) return st;
+  QuantParams p{static_cast<const uint16_t*>(x), M, K, q, s, qT, sT, dev->wait_ns, 0u, 0u};
+  return launch_quant(p, false, kScaleMx32, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_mx_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb, int64_t M, int64_t N,
+                         int64_t K, void* C, bfp8_stream_t stream) {
+  if (!A || !sa || !B || !sb || !C) return BFP8_EINVAL;
+  if (!dim_ok(M) || !dim_ok(N) || !dim_ok(K)) return BFP8_EINVAL;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sa) || !aligned16(sb) || !aligned16(C)) return BFP8_EALIGN;
+  DeviceState* dev = nullptr;
+  bfp8_status s = device_state(&dev);
+  if (s != BFP8_OK) return s;
+  CUtensorMap ta, tb, tc;
+  if ((s = make_kmajor_tmap(&ta, A, M, K, 128)) != BFP8_OK) return s;
+  if ((s = make_kmajor_tmap(&tb, B, N, K, 128)) != BFP8_OK) return s;
+  if ((s = make_bf16_store_tmap(&tc, C, M, N, true)) != BFP8_OK) return s;
+  GemmParams p{};
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_tiles = static_cast<int>(M / 128);
+  p.n_tiles = static_cast<int>(N / 128);
+  p.tiles = p.m_tiles * p.n_tiles;
+  p.splits = 1;
+  p.kps = static_cast<int>(K / 128);
+  p.units = p.tiles;
+  p.group_m = 16;
+  p.m_tile_rows = 128;
+  p.sa = sa;
+  p.sb = sb;
+  p.C = static_cast<uint16_t*>(C);
+  p.wait_ns = dev->wait_ns;
+  p.stall = take_stall();
+  const int grid = std::min(p.units, dev->sms);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  mx_gemm_kernel<<<grid, kGemmThreads, MxSmem::kAlloc, st>>>(ta, tb, tc, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cuda_status(cudaGetLastError());
 }
 
 size_t bfp8_gemm_workspace_bytes(bfp8_layout layout, int64_t M, int64_t N, int64_t K) {

@@ -296,19 +296,39 @@ __device__ __forceinline__ GroupScale make_group_scale_recip(float amax) {
 constexpr int kScaleAmax448 = 0;
 constexpr int kScalePow2 = 1;
 constexpr int kScaleMulRecip = 2;
+// MXFP8 1x32 recipe (bloombook.cn tutorial, FP8 paragraph and MXFP concept
+// figure: one shared scale per 32 consecutive values): groups of 32 instead
+// of 128, each with the power-of-two scale above clamped to the E8M0 range
+// [2^-127, 2^127].  Not a mode of the C ABI's bfp8_scale_mode: its scales
+// have their own layout ([C/32, R]), so it has its own entry point.
+constexpr int kScaleMx32 = 3;
+
+// The power-of-two scale clamped to 2^-127 from below (the upper end, 2^127,
+// lies beyond any bf16 amax / 448).  2^-127 is an fp32 subnormal whose
+// reciprocal 2^127 is normal, so every group is on the multiply path.
+__device__ __forceinline__ GroupScale make_group_scale_mx(float amax) {
+  GroupScale g = make_group_scale_pow2(amax);
+  if (g.s < 0x1p-127f) {
+    g.s = 0x1p-127f;
+    g.r = 0x1p+127f;
+    g.exact = true;
+  }
+  return g;
+}
 
 // Whether a group scale of the given mode is on the fast (multiply or FMA)
 // path; restates GroupScale::exact from s alone.
 template <int kScale>
 __device__ __forceinline__ bool scale_fast(float s) {
   if constexpr (kScale == kScalePow2) return s >= 0x1p-127f;
-  if constexpr (kScale == kScaleMulRecip) return true;
+  if constexpr (kScale == kScaleMulRecip || kScale == kScaleMx32) return true;
   return s >= 0x1p-80f && s <= 0x1p+100f;
 }
 
 template <int kScale>
 __device__ __forceinline__ GroupScale make_scale(float amax) {
   if constexpr (kScale == kScalePow2) return make_group_scale_pow2(amax);
+  if constexpr (kScale == kScaleMx32) return make_group_scale_mx(amax);
   if constexpr (kScale == kScaleMulRecip) return make_group_scale_recip(amax);
   return make_group_scale(amax);
 }

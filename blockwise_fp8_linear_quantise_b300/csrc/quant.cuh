@@ -215,6 +215,7 @@ template <bool kWeight, int kMode, int kScale, bool kGlu>
 __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
     quantize_tile_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   static_assert(!(kGlu && kWeight), "the SiLU-gated prologue quantises an activation");
+  static_assert(kScale != kScaleMx32 || (!kWeight && !kGlu), "the 1x32 recipe has no 2-D blocks or prologue");
   using L = QuantLayout<kGlu>;
   constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -349,6 +350,48 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
       quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + sf * L::kSlot, &full[sf], lane);
       fill.advance(step, drt, dct, ctiles);
       ++issued;
+    }
+
+    if constexpr (kScale == kScaleMx32) {
+      // MXFP8 1x32 groups.  Row view: 32-group m of a row is columns
+      // 32m .. 32m + 31, whose halves 16h .. 16h + 15 sit in the two lanes of
+      // the row's lane pair.  Column view: a column's 32-row group k (rows
+      // 32k ..) sits in lanes (cq, k) and (cq, k + 4), 16 lanes apart.
+      if constexpr (kRows) {
+        uint8_t* qrow = p.q + (r0 + wrow) * p.C + c0 + 16 * hh;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint4 a = rv[2 * m], b = rv[2 * m + 1];
+          const uint32_t m2 = bf16x2_maxabs(bf16x2_maxabs(bf16x2_maxabs(a.x, a.y), bf16x2_maxabs(a.z, a.w)),
+                                            bf16x2_maxabs(bf16x2_maxabs(b.x, b.y), bf16x2_maxabs(b.z, b.w)));
+          float am = bf16x2_absmax(m2);
+          am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+          const GroupScale gs = make_group_scale_mx(am);
+          if (hh == (m & 1)) p.s[(static_cast<int64_t>(cur.ct) * 4 + m) * p.R + r0 + wrow] = gs.s;
+          *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<true, kScaleMx32>(a, b, gs);
+        }
+      }
+      if constexpr (kCols) {
+        uint32_t c01 = 0u, c23 = 0u;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          c01 = bf16x2_maxabs(c01, cv[k].x);
+          c23 = bf16x2_maxabs(c23, cv[k].y);
+        }
+        c01 = bf16x2_maxabs(c01, __shfl_xor_sync(0xffffffffu, c01, 16));
+        c23 = bf16x2_maxabs(c23, __shfl_xor_sync(0xffffffffu, c23, 16));
+        const GroupScale gs0 = make_group_scale_mx(fabsf(bf16lo(c01))), gs1 = make_group_scale_mx(fabsf(bf16hi(c01)));
+        const GroupScale gs2 = make_group_scale_mx(fabsf(bf16lo(c23))), gs3 = make_group_scale_mx(fabsf(bf16hi(c23)));
+        if (g < 4)  // the 4 scales of this lane's columns for 32-group g of the tile's rows
+          *reinterpret_cast<float4*>(p.sT + (static_cast<int64_t>(cur.rt) * 4 + g) * p.C + c0 + 16 * warp + 4 * cq) =
+              make_float4(gs0.s, gs1.s, gs2.s, gs3.s);
+        uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
+        *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, true, kScaleMx32>(cv, gs0);
+        *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1, true, kScaleMx32>(cv, gs1);
+        *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0, true, kScaleMx32>(cv, gs2);
+        *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1, true, kScaleMx32>(cv, gs3);
+      }
+      continue;
     }
 
     // amaxes (packed bf16, NaN ignored)

@@ -142,6 +142,45 @@ def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, st
     return q, qT, s
 
 
+def quantize_mx_1x32(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=None, stream=None):
+    """MXFP8 1x32 quantisation of bf16 x [M, K] (power-of-two scales per 32 values).
+
+    rows   -> q [M, K] uint8 (groups of 32 along K), s [K/32, M] float32
+    tokens -> qT [K, M] uint8 (groups of 32 rows per column), sT [M/32, K]
+    Returns (q, s, qT, sT) with None for outputs not requested.
+    """
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    if rows:
+        q = _out(q, torch.uint8, (M, K), x.device, "q")
+        s = _out(s, torch.float32, (K // 32, M), x.device, "s")
+    else:
+        q = s = None
+    if tokens:
+        qT = _out(qT, torch.uint8, (K, M), x.device, "qT")
+        sT = _out(sT, torch.float32, (M // 32, K), x.device, "sT")
+    else:
+        qT = sT = None
+    _check(_lib.load().bfp8_quantize_mx_1x32(_ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _stream(stream)),
+           "quantize_mx_1x32")
+    return q, s, qT, sT
+
+
+def mx_gemm(A, sa, B, sb, C=None, stream=None):
+    """C [M, N] bf16 = A . B^T with 1x32 scales along K for both operands (A [M, K], sa [K/32, M], B [N, K],
+    sb [K/32, N])."""
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, torch.uint8, (M, K), "A")
+    _need(B, torch.uint8, (N, K), "B")
+    _need(sa, torch.float32, (K // 32, M), "sa")
+    _need(sb, torch.float32, (K // 32, N), "sb")
+    C = _out(C, torch.bfloat16, (M, N), A.device, "C")
+    _check(_lib.load().bfp8_mx_gemm(_ptr(A), _ptr(sa), _ptr(B), _ptr(sb), M, N, K, _ptr(C), _stream(stream)),
+           "mx_gemm")
+    return C
+
+
 def gemm_workspace_bytes(layout, M, N, K):
     return int(_lib.load().bfp8_gemm_workspace_bytes(layout, M, N, K))
 

@@ -163,6 +163,42 @@ bfp8_status bfp8_swiglu_quantize_1x128(const void* gu, int64_t M, int64_t F, voi
                                        bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
+ * MXFP8 1x32 recipe, the finer-grained scaling that the blockwise recipe is
+ * compared with (bloombook.cn tutorial, FP8 paragraph and MXFP concept figure:
+ * every 32 consecutive values share one scale X, and a code decodes as
+ * V_i = Q_i * X; section 3.2 of the paper runs its own recipe through that
+ * hardware path on SM120 with power-of-two scales).
+ *
+ * bfp8_quantize_mx_1x32: groups of 32 instead of 128, for activations,
+ * gradients and weights alike (the recipe has no 2-D blocks).
+ *   x   bf16 [M, K], read only.
+ *   q   E4M3 [M, K] or NULL: groups of 32 along K;  s fp32 [K/32, M].
+ *   qT  E4M3 [K, M] or NULL: groups of 32 consecutive rows per column,
+ *       stored transposed;  sT fp32 [M/32, K].
+ * Scale of a group: s = 2^k, the smallest power of two >= amax/448, with k
+ * clamped to the E8M0 range [-127, 127] (only the lower end is ever reached);
+ * 1 for an all-zero group.  Codes: q = E4M3_rn_satfinite(x / s), an exact
+ * scaling.  At least one of q / qT.  Errors: EINVAL, EALIGN, ECUDA.
+ *
+ * bfp8_mx_gemm: C bf16 [M, N] = bf16( sum over 32-deep slices t of
+ *   P_t[i, j] * sa(i, t) * sb(j, t) ), P_t the tensor-core fp32 sum of the
+ *   slice's products, promoted in fp32 slice by slice.
+ *   A E4M3 [M, K], sa fp32 [K/32, M];  B E4M3 [N, K], sb fp32 [K/32, N]:
+ *   both as bfp8_quantize_mx_1x32 returns them in either direction.  For a
+ *   linear layer Y = X . W^T: FPROP A = q(X), B = q(W); DGRAD A = q(dY),
+ *   B = qT(W) (W^T quantised along the output features); WGRAD A = qT(dY),
+ *   B = qT(X).  M, N, K positive multiples of 128.  Errors: EINVAL, EALIGN,
+ *   EUNSUPPORTED, ECUDA.
+ */
+bfp8_status bfp8_quantize_mx_1x32(const void* x, int64_t M, int64_t K,
+                                  uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                  bfp8_stream_t stream);
+bfp8_status bfp8_mx_gemm(const uint8_t* A, const float* sa,
+                         const uint8_t* B, const float* sb,
+                         int64_t M, int64_t N, int64_t K,
+                         void* C, bfp8_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM with fp32 promotion per 128-deep slice (section 3.2:
  * E4M3 operands, fp32 training state; scales per 1x128 group / 128x128 block).
  *
@@ -179,7 +215,8 @@ bfp8_status bfp8_swiglu_quantize_1x128(const void* gu, int64_t M, int64_t F, voi
  *   C    bf16 [M, N], written.
  *   Cq / sCq  optional fused quantised epilogue: E4M3 [M, N] codes of the
  *        bf16 C in 1x128 groups along N, with fp32 scales [N/128, M], exactly
- *        as bfp8_quantize_act_1x128 would produce from C.  Both or neither.
+ *        as bfp8_quantize_act_1x128 (the default amax/448 rule; there is no
+ *        scale-mode variant) would produce from C.  Both or neither.
  *   workspace / ws_bytes  scratch of at least bfp8_gemm_workspace_bytes()
  *        bytes (may be 0 bytes, then workspace may be NULL).
  * Errors: EINVAL, EALIGN, EWORKSPACE, EUNSUPPORTED, ECUDA.
