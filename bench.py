@@ -94,7 +94,7 @@ def strip_comments(src):
 def kernel_source_hash():
     """Hash of the kernel sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
-    for f in ("common.cuh", "gemm.cuh", "quant.cuh", "api.cu"):
+    for f in ("common.cuh", "gemm.cuh", "gemm_mx.cuh", "quant.cuh", "api.cu"):
         with open(os.path.join(ROOT, "blockwise_fp8_linear_quantise_b300", "csrc", f), encoding="utf-8") as fh:
             h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -127,6 +127,9 @@ def parse_args(argv=None):
                     help="time the SiLU-gated prologue (bfp8_swiglu_quantize_1x128) on the down projection's input")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
+    ap.add_argument("--oracle-plan", action="store_true",
+                    help="time the CPU oracle on every configuration in full (stack28: layer 0 in full, 1/16 of the "
+                         "output tiles of layers 1-27, extrapolated) against the GPU path, checking parity")
     ap.add_argument("--probe-mx", action="store_true",
                     help="compare the MXFP8 1x32 recipe with the blockwise one on the mlp_down layer: accuracy of "
                          "every GEMM against the unquantised product, and time of quantisers and GEMMs")
@@ -837,6 +840,129 @@ def fp8_peak_probe():
     return 0
 
 
+def oracle_plan(args):
+    """The oracle timing plan: the CPU oracle, on every host core, against the
+    GPU path on the same CPU-drawn inputs of every configuration.
+
+    tiny, mlp_gateup, mlp_down, attn_proj: every quantisation and every GEMM
+    of the configuration in full.  stack28: every layer's quantisations in
+    full; layer 0's GEMMs in full; for layers 1-27 a seeded sample of 1/16 of
+    each GEMM's 128 x 128 output tiles (a quarter of the 128-row blocks times
+    a quarter of the 128-column blocks), whose oracle time is extrapolated to
+    the whole GEMM and labelled so.  Parity is checked wherever the oracle ran:
+    codes and scales bit for bit, GEMM bf16 outputs within relative Frobenius
+    error 1e-3.  One JSON line per configuration."""
+    import numpy as np
+    import torch
+    from blockwise_fp8_linear_quantise_b300 import ops, workloads
+    from oracle import parallel
+    cores = oracle_cores()
+    host = host_info()
+    np32 = lambda t: t.float().cpu().numpy()
+    u8 = lambda t: t.cpu().numpy()
+
+    def same(got, want, what):
+        g, w = np.asarray(got), np.asarray(want)
+        if g.dtype == np.float32:
+            g, w = g.view(np.uint32), w.view(np.uint32)
+        if not np.array_equal(g, w):
+            raise SystemExit(f"oracle plan: {what} differs from the oracle")
+
+    def rel(g, w):
+        w = np.asarray(w, np.float64)
+        return float(np.linalg.norm(np.asarray(g, np.float64) - w) / max(np.linalg.norm(w), 1e-300))
+
+    gpu_q = {}
+
+    def quant(kind, t, key):
+        """GPU and oracle quantisation of one tensor; returns the oracle's outputs."""
+        if key in gpu_q:
+            return gpu_q[key]
+        x = t.to("cuda")
+        t0 = time.perf_counter()
+        if kind == "w":
+            o = parallel.quantize_w_128x128(np32(t))
+            g = ops.quantize_w_128x128(x)
+            nbytes = t.numel() * (4 + 4 / 16384)
+        else:
+            o = parallel.quantize_act_1x128(np32(t)) + parallel.quantize_act_tokens_1x128(np32(t))
+            g = ops.quantize_act_1x128(x, rows=True, tokens=True)
+            nbytes = t.numel() * (4 + 8 / 128)
+        dt = time.perf_counter() - t0
+        assert ops.sync_status() == 0
+        for gi, oi, nm in zip(g, o, ("q", "s", "qT", "sT") if kind != "w" else ("Wq", "WqT", "sW")):
+            same(u8(gi), oi, f"{key} {nm}")
+        stats["quant_s"] += dt
+        stats["quant_bytes"] += nbytes
+        gpu_q[key] = (g, o)
+        return g, o
+
+    rng = np.random.default_rng(2024)
+    for name in ("tiny", "mlp_gateup", "mlp_down", "attn_proj", "stack28"):
+        wl = workloads.make(name)
+        gpu_q.clear()
+        stats = {"quant_s": 0.0, "quant_bytes": 0.0, "gemm_s_full": 0.0, "gemm_flop_full": 0.0,
+                 "gemm_s_sampled": 0.0, "gemm_flop_sampled": 0.0, "gemm_s_extrapolated": 0.0, "worst_rel_fro": 0.0,
+                 "gemms_full": 0, "gemms_sampled": 0}
+        cache = {}
+        tens = lambda tag, layer=None: cache.setdefault((tag, layer), workloads.tensor(wl, tag, layer))
+        for s in wl.linears:
+            li = workloads.layer_of(s)
+            sampled = name == "stack28" and li > 0
+            (Xq, sX, XqT, sXT), (oXq, osX, oXqT, osXT) = quant("a", tens(s.x_tag), s.x_tag)
+            (Wq, WqT, sW), (oWq, oWqT, osW) = quant("w", tens(s.w_tag, li), f"{s.w_tag}@{li}")
+            gemms = [("fprop", ops.FPROP, (Xq, sX, Wq, sW), (oXq, osX, oWq, osW), s.M, s.N, s.K)]
+            if s.backward:
+                (dYq, sdY, dYqT, sdYT), (odYq, osdY, odYqT, osdYT) = quant("a", tens(s.dy_tag), s.dy_tag)
+                gemms += [("dgrad", ops.DGRAD, (dYq, sdY, WqT, sW), (odYq, osdY, oWqT, osW), s.M, s.K, s.N),
+                          ("wgrad", ops.WGRAD, (dYqT, sdYT, XqT, sXT), (odYqT, osdYT, oXqT, osXT), s.N, s.K, s.M)]
+            for gname, lay, gargs, oargs, M, N, K in gemms:
+                C = np32(ops.fp8_block_gemm(lay, *gargs))
+                assert ops.sync_status() == 0
+                rows = cols = None
+                if sampled:
+                    rb = np.sort(rng.choice(M // 128, max(1, M // 512), replace=False))
+                    cb = np.sort(rng.choice(N // 128, max(1, N // 512), replace=False))
+                    rows = (rb[:, None] * 128 + np.arange(128)).ravel()
+                    cols = (cb[:, None] * 128 + np.arange(128)).ravel()
+                t0 = time.perf_counter()
+                _, want = parallel.gemm_rows(gname, *oargs, rows=rows, cols=cols)
+                dt = time.perf_counter() - t0
+                got = C if rows is None else C[np.ix_(rows, cols)]
+                err = rel(got, want)
+                if not err <= 1e-3:
+                    raise SystemExit(f"oracle plan: {name} {s.name} {gname} relative Frobenius error {err:.3e}")
+                stats["worst_rel_fro"] = max(stats["worst_rel_fro"], err)
+                flop = 2.0 * M * N * K
+                if rows is None:
+                    stats["gemm_s_full"] += dt
+                    stats["gemm_flop_full"] += flop
+                    stats["gemms_full"] += 1
+                else:
+                    frac = len(rows) * len(cols) / (M * N)
+                    stats["gemm_s_sampled"] += dt
+                    stats["gemm_flop_sampled"] += flop * frac
+                    stats["gemm_s_extrapolated"] += dt / frac
+                    stats["gemms_sampled"] += 1
+        line = {"oracle_plan": name, "cores": cores, **host,
+                "quantisers": {"oracle_s": round(stats["quant_s"], 2),
+                               "oracle_GB_per_s": round(stats["quant_bytes"] / max(stats["quant_s"], 1e-9) / 1e9, 3),
+                               "tensors": len(gpu_q), "parity": "bit-exact (codes and scales)"},
+                "gemms_full": {"count": stats["gemms_full"], "oracle_s": round(stats["gemm_s_full"], 2),
+                               "oracle_TFLOP_per_s": round(stats["gemm_flop_full"] / max(stats["gemm_s_full"], 1e-9)
+                                                           / 1e12, 4)},
+                "worst_rel_fro_vs_oracle": stats["worst_rel_fro"]}
+        if stats["gemms_sampled"]:
+            line["gemms_sampled_1_in_16_tiles"] = {
+                "count": stats["gemms_sampled"], "oracle_s": round(stats["gemm_s_sampled"], 2),
+                "oracle_TFLOP_per_s": round(stats["gemm_flop_sampled"] / max(stats["gemm_s_sampled"], 1e-9) / 1e12, 4),
+                "oracle_s_for_all_tiles_extrapolated": round(stats["gemm_s_extrapolated"], 1)}
+        print(json.dumps(line), flush=True)
+        del cache
+        torch.cuda.empty_cache()
+    return 0
+
+
 def mx_probe(args):
     """The MXFP8 1x32 recipe against the blockwise 1x128 / 128x128 recipe on
     the mlp_down layer (X [8192, 6144], W [2048, 6144], dY [8192, 2048]):
@@ -950,6 +1076,8 @@ def main(argv=None):
         return swiglu_probe(args)
     if args.probe_mx:
         return mx_probe(args)
+    if args.oracle_plan:
+        return oracle_plan(args)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

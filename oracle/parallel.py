@@ -71,20 +71,26 @@ def _ready(_):
     return os.getpid()
 
 
-def _cols_job(fn_name, A, sa, B, sb, cols):
-    return getattr(gemm, fn_name)(A, sa, B, sb, cols=cols)
+def _cols_job(fn_name, A, sa, B, sb, rows, cols):
+    return getattr(gemm, fn_name)(A, sa, B, sb, rows=rows, cols=cols)
 
 
-def gemm_rows(fn_name, A, sa, B, sb):
-    """gemm.<fn_name>(A, sa, B, sb) computed as one block of output columns
-    (rows of B, which each worker alone decodes) per worker; returns (acc,
-    out) exactly as the serial call does."""
+def gemm_rows(fn_name, A, sa, B, sb, rows=None, cols=None):
+    """gemm.<fn_name>(A, sa, B, sb, rows, cols) computed as one block of
+    output rows or columns per worker, whichever operand is larger being the
+    one split (each worker decodes only its block of it); returns (acc, out)
+    exactly as the serial call does."""
     p = pool()
-    n = np.asarray(B).shape[0]
-    blocks = [b for b in np.array_split(np.arange(n), min(n, _WORKERS)) if len(b)]
-    futs = [p.submit(_cols_job, fn_name, A, sa, B, sb, b) for b in blocks]
+    rows = np.arange(np.asarray(A).shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(np.asarray(B).shape[0]) if cols is None else np.asarray(cols)
+    by_rows = len(rows) > len(cols)
+    split = rows if by_rows else cols
+    blocks = [b for b in np.array_split(split, min(len(split), _WORKERS)) if len(b)]
+    futs = [p.submit(_cols_job, fn_name, A, sa, B, sb, b if by_rows else rows, cols if by_rows else b)
+            for b in blocks]
     parts = [f.result() for f in futs]
-    return np.hstack([a for a, _ in parts]), np.hstack([o for _, o in parts])
+    join = np.vstack if by_rows else np.hstack
+    return join([a for a, _ in parts]), join([o for _, o in parts])
 
 
 def _blocks(n, unit):

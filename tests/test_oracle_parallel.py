@@ -31,5 +31,11 @@ def test_pool_matches_serial_oracle_bit_for_bit():
         acc1, _ = gemm.fprop(*[s1[k] for k in ("Xq", "sX", "Wq", "sW")])
         acc2, _ = parallel.gemm_rows("fprop", *[s1[k] for k in ("Xq", "sX", "Wq", "sW")])
         assert np.array_equal(acc1.view(np.uint32), acc2.view(np.uint32))
+        # subsets of rows and columns (the tile samples of the oracle timing plan), split either way
+        for rows, cols in ((np.arange(128, 384), np.arange(0, 128)), (np.arange(0, 128), np.arange(0, 256))):
+            a1, o1 = gemm.fprop(*[s1[k] for k in ("Xq", "sX", "Wq", "sW")], rows=rows, cols=cols)
+            a2, o2 = parallel.gemm_rows("fprop", *[s1[k] for k in ("Xq", "sX", "Wq", "sW")], rows=rows, cols=cols)
+            assert np.array_equal(a1.view(np.uint32), a2.view(np.uint32))
+            assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
     finally:
         parallel.shutdown()
