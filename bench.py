@@ -127,6 +127,8 @@ def parse_args(argv=None):
                     help="time the SiLU-gated prologue (bfp8_swiglu_quantize_1x128) on the down projection's input")
     ap.add_argument("--probe-fp8-peak", action="store_true",
                     help="time the library FP8 GEMM (torch._scaled_mm, per-tensor scales, 8192^3) as a peak reference")
+    ap.add_argument("--plan-configs", default="tiny,mlp_gateup,mlp_down,attn_proj,stack28",
+                    help="--oracle-plan: the configurations to run, comma-separated")
     ap.add_argument("--oracle-plan", action="store_true",
                     help="time the CPU oracle on every configuration in full (stack28: layer 0 in full, 1/16 of the "
                          "output tiles of layers 1-27, extrapolated) against the GPU path, checking parity")
@@ -898,7 +900,7 @@ def oracle_plan(args):
         return g, o
 
     rng = np.random.default_rng(2024)
-    for name in ("tiny", "mlp_gateup", "mlp_down", "attn_proj", "stack28"):
+    for name in args.plan_configs.split(","):
         wl = workloads.make(name)
         gpu_q.clear()
         stats = {"quant_s": 0.0, "quant_bytes": 0.0, "gemm_s_full": 0.0, "gemm_flop_full": 0.0,
@@ -917,7 +919,7 @@ def oracle_plan(args):
                 gemms += [("dgrad", ops.DGRAD, (dYq, sdY, WqT, sW), (odYq, osdY, oWqT, osW), s.M, s.K, s.N),
                           ("wgrad", ops.WGRAD, (dYqT, sdYT, XqT, sXT), (odYqT, osdYT, oXqT, osXT), s.N, s.K, s.M)]
             for gname, lay, gargs, oargs, M, N, K in gemms:
-                C = np32(ops.fp8_block_gemm(lay, *gargs))
+                Cg = ops.fp8_block_gemm(lay, *gargs)
                 assert ops.sync_status() == 0
                 rows = cols = None
                 if sampled:
@@ -925,10 +927,12 @@ def oracle_plan(args):
                     cb = np.sort(rng.choice(N // 128, max(1, N // 512), replace=False))
                     rows = (rb[:, None] * 128 + np.arange(128)).ravel()
                     cols = (cb[:, None] * 128 + np.arange(128)).ravel()
+                    Cg = Cg[torch.as_tensor(rows, device=Cg.device)][:, torch.as_tensor(cols, device=Cg.device)]
+                got = np32(Cg)
+                del Cg
                 t0 = time.perf_counter()
                 _, want = parallel.gemm_rows(gname, *oargs, rows=rows, cols=cols)
                 dt = time.perf_counter() - t0
-                got = C if rows is None else C[np.ix_(rows, cols)]
                 err = rel(got, want)
                 if not err <= 1e-3:
                     raise SystemExit(f"oracle plan: {name} {s.name} {gname} relative Frobenius error {err:.3e}")
@@ -944,6 +948,8 @@ def oracle_plan(args):
                     stats["gemm_flop_sampled"] += flop * frac
                     stats["gemm_s_extrapolated"] += dt / frac
                     stats["gemms_sampled"] += 1
+            if name == "stack28":
+                print(f"oracle plan: stack28 {s.name} done", file=sys.stderr, flush=True)
         line = {"oracle_plan": name, "cores": cores, **host,
                 "quantisers": {"oracle_s": round(stats["quant_s"], 2),
                                "oracle_GB_per_s": round(stats["quant_bytes"] / max(stats["quant_s"], 1e-9) / 1e9, 3),

@@ -8,7 +8,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libbfp8.so")
 SOURCES = [os.path.join(HERE, "csrc", "api.cu")]
-DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("common.cuh", "quant.cuh", "gemm.cuh")] + [
+DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("common.cuh", "quant.cuh", "gemm.cuh", "gemm_mx.cuh")] + [
     os.path.join(ROOT, "include", "bfp8.h")]
 
 NVCC_FLAGS = [

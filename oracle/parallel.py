@@ -21,6 +21,7 @@ that has already used a GPU can hang.
 import concurrent.futures as cf
 import multiprocessing as mp
 import os
+from multiprocessing import shared_memory
 
 import numpy as np
 
@@ -71,24 +72,53 @@ def _ready(_):
     return os.getpid()
 
 
-def _cols_job(fn_name, A, sa, B, sb, rows, cols):
-    return getattr(gemm, fn_name)(A, sa, B, sb, rows=rows, cols=cols)
+def _attach(desc):
+    """A read-only numpy view of an operand the parent placed in shared
+    memory, and the segment (to close once the view is no longer used)."""
+    name, shape, dtype = desc
+    shm = shared_memory.SharedMemory(name=name)
+    a = np.ndarray(shape, dtype=dtype, buffer=shm.buf)
+    a.flags.writeable = False
+    return a, shm
+
+
+def _cols_job(fn_name, descs, rows, cols):
+    views = [_attach(d) for d in descs]
+    try:
+        acc, out = getattr(gemm, fn_name)(*[v for v, _ in views], rows=rows, cols=cols)
+        return np.array(acc), np.array(out)  # copies: nothing refers to the segments afterwards
+    finally:
+        for _, shm in views:
+            shm.close()
 
 
 def gemm_rows(fn_name, A, sa, B, sb, rows=None, cols=None):
     """gemm.<fn_name>(A, sa, B, sb, rows, cols) computed as one block of
     output rows or columns per worker, whichever operand is larger being the
     one split (each worker decodes only its block of it); returns (acc, out)
-    exactly as the serial call does."""
+    exactly as the serial call does.  The operands reach the workers through
+    shared memory (one copy in all), not pickled once per worker."""
     p = pool()
-    rows = np.arange(np.asarray(A).shape[0]) if rows is None else np.asarray(rows)
-    cols = np.arange(np.asarray(B).shape[0]) if cols is None else np.asarray(cols)
+    ops = [np.ascontiguousarray(x) for x in (A, sa, B, sb)]
+    rows = np.arange(ops[0].shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(ops[2].shape[0]) if cols is None else np.asarray(cols)
     by_rows = len(rows) > len(cols)
     split = rows if by_rows else cols
     blocks = [b for b in np.array_split(split, min(len(split), _WORKERS)) if len(b)]
-    futs = [p.submit(_cols_job, fn_name, A, sa, B, sb, b if by_rows else rows, cols if by_rows else b)
-            for b in blocks]
-    parts = [f.result() for f in futs]
+    segs = []
+    try:
+        descs = []
+        for x in ops:
+            shm = shared_memory.SharedMemory(create=True, size=max(x.nbytes, 1))
+            segs.append(shm)
+            np.ndarray(x.shape, dtype=x.dtype, buffer=shm.buf)[...] = x
+            descs.append((shm.name, x.shape, x.dtype.str))
+        futs = [p.submit(_cols_job, fn_name, descs, b if by_rows else rows, cols if by_rows else b) for b in blocks]
+        parts = [f.result() for f in futs]
+    finally:
+        for shm in segs:
+            shm.close()
+            shm.unlink()
     join = np.vstack if by_rows else np.hstack
     return join([a for a, _ in parts]), join([o for _, o in parts])
 
