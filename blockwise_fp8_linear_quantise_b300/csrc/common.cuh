@@ -226,8 +226,11 @@ __device__ __forceinline__ float group_scale(float amax) {
 // mantissas, every x in (0, amax]), Q equals fp32_rn(x / s) every time, and y0
 // alone misses some codes.  Quotients below 2^-11 (codes +-0) stay below the
 // smallest E4M3 rounding boundary (2^-10) whatever the remainder's rounding.
-// The sign of a zero quotient is restored from x.  A group whose scale lies
-// outside [2^-80, 2^100] (or is not finite) takes the IEEE division.
+// The quantisers write the step on -x, which keeps the sign of a zero
+// quotient (quotient_pair_neg); the GEMM's quantised epilogue restores it
+// from x.  A group whose scale lies outside [2^-80, 2^100] (or is not
+// finite) takes the power-of-two pre-scaling in the quantisers
+// (scaled_group) and the IEEE division in the epilogue.
 struct GroupScale {
   float s;     // dequantisation scale amax/448 (1 for an all-zero group)
   float r;     // RN(1/s)
@@ -347,6 +350,24 @@ __device__ __forceinline__ float2 quotient_pair_unsigned_zero(float2 x, float2 r
   return ffma2(ffma2(y0, ns2, x), r2, y0);
 }
 
+// -x, widened to fp32, for the bf16 value in the low / high half of w: the
+// sign bit is flipped by the same integer operation that places the value.
+__device__ __forceinline__ float neg_bf16lo(uint32_t w) { return __uint_as_float((w << 16) + 0x80000000u); }
+__device__ __forceinline__ float neg_bf16hi(uint32_t w) { return __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u); }
+
+// The correction step written on nx = -x, with nr2 = -RN(1/s) and s2 = s in
+// both components:
+//   y0 = RN(nx nr)        = RN(x r), the same product;
+//   e  = RN(s y0 + nx)    = -(x - s y0), exact as before;
+//   Q  = RN(e nr + y0)    = RN(y0 + r (x - s y0)), the same sum.
+// So Q is RN(x / s) wherever the step on x gives it, and for x = -0 the last
+// sum adds two zeros of x's sign (-0 + -0), so Q keeps the sign of every
+// zero without a separate restore.
+__device__ __forceinline__ float2 quotient_pair_neg(float2 nx, float2 nr2, float2 s2) {
+  const float2 y0 = fmul2(nx, nr2);
+  return ffma2(ffma2(y0, s2, nx), nr2, y0);
+}
+
 // Four E4M3 codes (byte i from q_i) in one register: two paired casts and
 // one pack.
 __device__ __forceinline__ uint32_t e4m3x4(float q0, float q1, float q2, float q3) {
@@ -360,25 +381,43 @@ __device__ __forceinline__ uint32_t e4m3x4(float q0, float q1, float q2, float q
   return r;
 }
 
-// Codes of the four bf16 values of words w0, w1 (value 2i in the low half of
-// word i) in one group on the FMA path, byte k = value k.  The quotient has
-// the sign of x (s > 0), so the sign bits of the four inputs are ORed into
-// the codes: that restores -0 and changes nothing else.
-__device__ __forceinline__ uint32_t quant4_exact(uint32_t w0, uint32_t w1, float2 r2, float2 ns2) {
-  const float2 q0 = quotient_pair_unsigned_zero(make_float2(bf16lo(w0), bf16hi(w0)), r2, ns2);
-  const float2 q1 = quotient_pair_unsigned_zero(make_float2(bf16lo(w1), bf16hi(w1)), r2, ns2);
-  const uint32_t signs = __byte_perm(w0, w1, 0x7531) & 0x80808080u;
-  return e4m3x4(q0.x, q0.y, q1.x, q1.y) | signs;
+// State of a group whose scale is off the FMA path (s outside [2^-80, 2^100]
+// or not finite).  x / s = (x p) / (s p) for a power of two p, and s p lies
+// well inside that range: p = 2^100 for small s, 2^-64 for large.  x p is
+// exact unless it underflows, which happens only for s > 2^100 and
+// |x| < 2^-62, where |x / s| < 2^-162 and the code is a signed zero either
+// way.  The scaled pair takes two correction steps (a faithful quotient,
+// then Markstein's step), which give RN(x p / (s p)) for any normal s p.  An
+// infinite s (an infinite amax) takes p = 0: x p is then a signed zero for
+// finite x (code +-0, as x / inf) and NaN for infinite or NaN x (code NaN,
+// as inf / inf), and s p = 1 leaves it as it is.
+struct ScaledGroup {
+  float p;   // the power of two (0 for an infinite s)
+  float s;   // s p (1 for an infinite s)
+  float nr;  // -RN(1 / (s p))
+};
+
+__device__ __forceinline__ ScaledGroup scaled_group(float s) {
+  ScaledGroup g;
+  if (!(s <= 0x1.FFFFFEp+127f)) {
+    g.p = 0.0f;
+    g.s = 1.0f;
+    g.nr = -1.0f;
+    return g;
+  }
+  g.p = s < 1.0f ? 0x1p+100f : 0x1p-64f;
+  g.s = s * g.p;
+  g.nr = -__frcp_rn(g.s);
+  return g;
 }
 
-// Codes of the four bf16 values of words w0, w1 from their products with a
-// positive group multiplier (r2 = m in both halves): E4M3(fp32_rn(x * m)).
-// Under a power-of-two scale (m = 2^-k) the product is exact.  It keeps the
-// sign of a zero, so no sign restore is needed.
-__device__ __forceinline__ uint32_t quant4_mul(uint32_t w0, uint32_t w1, float2 r2) {
-  const float2 a = fmul2(make_float2(bf16lo(w0), bf16hi(w0)), r2);
-  const float2 b = fmul2(make_float2(bf16lo(w1), bf16hi(w1)), r2);
-  return e4m3x4(a.x, a.y, b.x, b.y);
+// RN(x / s) for the pair nx = -x of a group off the FMA path (see above).
+__device__ __forceinline__ float2 quotient_pair_scaled(float2 nx, const ScaledGroup& g) {
+  const float2 p2 = make_float2(g.p, g.p), s2 = make_float2(g.s, g.s), nr2 = make_float2(g.nr, g.nr);
+  const float2 nxp = fmul2(nx, p2);
+  const float2 y0 = fmul2(nxp, nr2);
+  const float2 y1 = ffma2(ffma2(y0, s2, nxp), nr2, y0);
+  return ffma2(ffma2(y1, s2, nxp), nr2, y1);
 }
 
 // Codes of the pair (x0, x1) (x0 in the low byte), one group on the FMA path.

@@ -23,12 +23,15 @@
 //     output chunks 2m+h (h = lane & 1), and
 //   * columns 16w..16w+15 (their groups of 128 rows: qT, sT): each lane holds
 //     4 columns over 16 consecutive rows.
-// It copies both slices into registers, releases the ring slot, reduces
-// amaxes with in-lane packed bf16 maxima and a few shuffles, turns each
-// amax into its scale and reciprocal once, forms every code from the
-// correctly rounded quotient (GroupScale), and stores codes straight to
-// global memory in 32-byte (rows) and 128-byte (columns) segments.  The
-// input is read from HBM once whichever outputs are requested.
+// It codes the row slice first and then the column slice, holding one of
+// them in registers at a time, and releases the ring slot as soon as the
+// last slice it needs is in registers.  For each slice it reduces amaxes
+// with in-lane packed bf16 maxima and a few shuffles, turns each amax into
+// its scale and reciprocal once, forms every code from the correctly
+// rounded quotient (GroupScale, written on -x so that zeros keep their
+// sign), and stores codes straight to global memory in 32-byte (rows) and
+// 128-byte (columns) segments.  The input is read from HBM once whichever
+// outputs are requested.
 //
 // Shared-memory image of a tile.  The input is addressed by TMA as the 2-D
 // tensor [R/16, 16 C]: its row y holds rows 16y..16y+15 of the input side by
@@ -107,60 +110,78 @@ __device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b) {
   return d;
 }
 
-// 16 codes of 8 words of bf16 pairs (value 2i in the low half of word i),
-// one group.  Groups with extreme scales (g.exact false) take the IEEE
-// division.
-template <int kScale>
-__device__ __forceinline__ uint4 quant16w(const uint32_t (&w)[8], const GroupScale& g) {
-  if (g.exact) {
-    const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-    if constexpr (kScale != kScaleAmax448)
-      return make_uint4(quant4_mul(w[0], w[1], r2), quant4_mul(w[2], w[3], r2), quant4_mul(w[4], w[5], r2),
-                        quant4_mul(w[6], w[7], r2));
-    else
-      return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
-                        quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
-  }
-  uint32_t c[8];
+// The 16 values of one group slice as a warp lane holds them.  Row slices:
+// value 2i + h is half h of word i.  Column slices: value k (row k) is half
+// kHalf of word kWord of the 8-byte chunk v[k].  neg(i) is -x_i and pos(i)
+// is x_i, widened to fp32 straight from the word that holds them.
+struct RowSlice {
+  const uint32_t (&w)[8];
+  __device__ __forceinline__ float neg(int i) const { return (i & 1) ? neg_bf16hi(w[i >> 1]) : neg_bf16lo(w[i >> 1]); }
+  __device__ __forceinline__ float pos(int i) const { return (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]); }
+};
+template <int kWord, int kHalf>
+struct ColSlice {
+  const uint2 (&v)[16];
+  __device__ __forceinline__ uint32_t word(int k) const { return kWord ? v[k].y : v[k].x; }
+  __device__ __forceinline__ float neg(int k) const { return kHalf ? neg_bf16hi(word(k)) : neg_bf16lo(word(k)); }
+  __device__ __forceinline__ float pos(int k) const { return kHalf ? bf16hi(word(k)) : bf16lo(word(k)); }
+};
+
+// 16 codes (byte i = value i) of a slice whose group scale g is on the fast
+// path: the correction step on -x (amax/448 mode) or one product with the
+// group multiplier (the other modes; exact for power-of-two scales).
+template <int kScale, class Slice>
+__device__ __forceinline__ uint4 codes16_fast(const Slice& v, const GroupScale& g) {
+  uint32_t c[4];
+  if constexpr (kScale == kScaleAmax448) {
+    const float2 nr2 = make_float2(-g.r, -g.r), s2 = make_float2(g.s, g.s);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) c[i] = quant_pair_div(bf16lo(w[i]), bf16hi(w[i]), g.s, g.s);
-  return make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16), c[6] | (c[7] << 16));
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = quotient_pair_neg(make_float2(v.neg(4 * i), v.neg(4 * i + 1)), nr2, s2);
+      const float2 b = quotient_pair_neg(make_float2(v.neg(4 * i + 2), v.neg(4 * i + 3)), nr2, s2);
+      c[i] = e4m3x4(a.x, a.y, b.x, b.y);
+    }
+  } else {
+    const float2 r2 = make_float2(g.r, g.r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = fmul2(make_float2(v.pos(4 * i), v.pos(4 * i + 1)), r2);
+      const float2 b = fmul2(make_float2(v.pos(4 * i + 2), v.pos(4 * i + 3)), r2);
+      c[i] = e4m3x4(a.x, a.y, b.x, b.y);
+    }
+  }
+  return make_uint4(c[0], c[1], c[2], c[3]);
 }
 
-// The same on the fast path only (every group of the tile has g.exact).
-template <int kScale>
-__device__ __forceinline__ uint4 quant16w_fast(const uint32_t (&w)[8], const GroupScale& g) {
-  const float2 r2 = make_float2(g.r, g.r), ns2 = make_float2(-g.s, -g.s);
-  if constexpr (kScale != kScaleAmax448)
-    return make_uint4(quant4_mul(w[0], w[1], r2), quant4_mul(w[2], w[3], r2), quant4_mul(w[4], w[5], r2),
-                      quant4_mul(w[6], w[7], r2));
-  else
-    return make_uint4(quant4_exact(w[0], w[1], r2, ns2), quant4_exact(w[2], w[3], r2, ns2),
-                      quant4_exact(w[4], w[5], r2, ns2), quant4_exact(w[6], w[7], r2, ns2));
+// The same for any group: groups off the fast path (extreme or infinite
+// scales) take the power-of-two pre-scaling and two correction steps.
+template <int kScale, class Slice>
+__device__ __forceinline__ uint4 codes16(const Slice& v, const GroupScale& g) {
+  if (g.exact) return codes16_fast<kScale>(v, g);
+  const ScaledGroup sg = scaled_group(g.s);
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = quotient_pair_scaled(make_float2(v.neg(4 * i), v.neg(4 * i + 1)), sg);
+    const float2 b = quotient_pair_scaled(make_float2(v.neg(4 * i + 2), v.neg(4 * i + 3)), sg);
+    c[i] = e4m3x4(a.x, a.y, b.x, b.y);
+  }
+  return make_uint4(c[0], c[1], c[2], c[3]);
 }
 
 // 16 codes of the 16 consecutive values in (a, b) (8 bf16 each), one group.
 template <bool kFast, int kScale>
 __device__ __forceinline__ uint4 quant16(const uint4& a, const uint4& b, const GroupScale& g) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  return kFast ? quant16w_fast<kScale>(w, g) : quant16w<kScale>(w, g);
-}
-
-// Values k and k+1 of one column (element kHalf of word kWord of row slices
-// k and k+1 in v[]) packed as one bf16 pair, row k in the low half.
-template <int kWord, int kHalf>
-__device__ __forceinline__ uint32_t col_pair(const uint2 (&v)[16], int k) {
-  const uint32_t w0 = kWord ? v[k].y : v[k].x, w1 = kWord ? v[k + 1].y : v[k + 1].x;
-  return kHalf ? __byte_perm(w0, w1, 0x7632) : __byte_perm(w0, w1, 0x5410);
+  const RowSlice v{w};
+  return kFast ? codes16_fast<kScale>(v, g) : codes16<kScale>(v, g);
 }
 
 // 16 codes of one column over 16 rows, one group.  Codes in row order.
 template <int kWord, int kHalf, bool kFast, int kScale>
-__device__ __forceinline__ uint4 quant_col16(const uint2 (&v)[16], const GroupScale& g) {
-  uint32_t w[8];
-#pragma unroll
-  for (int k = 0; k < 16; k += 2) w[k / 2] = col_pair<kWord, kHalf>(v, k);
-  return kFast ? quant16w_fast<kScale>(w, g) : quant16w<kScale>(w, g);
+__device__ __forceinline__ uint4 quant_col16(const uint2 (&cv)[16], const GroupScale& g) {
+  const ColSlice<kWord, kHalf> v{cv};
+  return kFast ? codes16_fast<kScale>(v, g) : codes16<kScale>(v, g);
 }
 
 // Warp 0 fetches tile (rt, ct) into ring slot `buf` with 32 TMA boxes (one
@@ -180,27 +201,22 @@ __device__ __forceinline__ void quant_fill(const CUtensorMap* tmx, uint32_t xrow
                 static_cast<int32_t>(rt * 8), bar);
 }
 
-// Codes of this warp's row and column slices of one tile, stored to global
-// memory.  kFast: every group scale of the warp is on the FMA path, so the
-// whole body is one branch-free block the compiler can interleave.
-template <int kMode, bool kFast, int kScale>
-__device__ __forceinline__ void quant_tile_codes(const uint4 (&rv)[8], const uint2 (&cv)[16], const GroupScale& grow,
-                                                 const GroupScale (&gc)[4], uint8_t* qrow, uint8_t* qcol,
-                                                 int64_t R) {
-  if constexpr ((kMode & kQRows) != 0) {
+// Codes of this lane's row slice (4 chunks of 16) under the row group scale.
+template <bool kFast, int kScale>
+__device__ __forceinline__ void quant_row_codes(const uint4 (&rv)[8], const GroupScale& g, uint8_t* qrow) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-      *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast, kScale>(rv[2 * m], rv[2 * m + 1], grow);
-  }
-  if constexpr ((kMode & kQCols) != 0) {
-    GroupScale g[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) g[k] = {gc[k].s, gc[k].r, kFast || scale_fast<kScale>(gc[k].s)};
-    *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast, kScale>(cv, g[0]);
-    *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast, kScale>(cv, g[1]);
-    *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast, kScale>(cv, g[2]);
-    *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast, kScale>(cv, g[3]);
-  }
+  for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(qrow + 32 * m) = quant16<kFast, kScale>(rv[2 * m], rv[2 * m + 1], g);
+}
+
+// Codes of this lane's 4 columns over its 16 rows (gc: their group scales),
+// column k to qcol + k R.
+template <bool kFast, int kScale>
+__device__ __forceinline__ void quant_col_codes(const uint2 (&cv)[16], const GroupScale (&gc)[4], uint8_t* qcol,
+                                                int64_t R) {
+  *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, kFast, kScale>(cv, gc[0]);
+  *reinterpret_cast<uint4*>(qcol + R) = quant_col16<0, 1, kFast, kScale>(cv, gc[1]);
+  *reinterpret_cast<uint4*>(qcol + 2 * R) = quant_col16<1, 0, kFast, kScale>(cv, gc[2]);
+  *reinterpret_cast<uint4*>(qcol + 3 * R) = quant_col16<1, 1, kFast, kScale>(cv, gc[3]);
 }
 
 // kWeight = false: activation groups (rows -> q/s, columns -> qT/sT).
@@ -281,9 +297,10 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
     uint8_t* buf = smem + s * L::kSlot;
     const int64_t r0 = static_cast<int64_t>(cur.rt) * 128, c0 = static_cast<int64_t>(cur.ct) * 128;
 
-    // both slices into registers, then hand the slot back
+    // The row view is coded before the column view is read, so that only
+    // one slice of the tile is held in registers at a time; the slot is
+    // handed back once the last slice this warp needs is in registers.
     uint4 rv[8];
-    uint2 cv[16];
     if constexpr (kRows || kGlu) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -334,22 +351,30 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
       mbar_arrive(&redbar[j & 1u]);
       if (!mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, p.wait_ns, 0x131u)) break;
     }
-    if constexpr (kCols) {
+
+    // Hands the slot back (every lane's reads of it are done) and lets warp 0
+    // refill the slot of tile j-1 (every warp released it, usually long ago)
+    // with tile j-1+kQStages.  False if that wait expired.
+    auto release = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (warp == 0 && j >= 1 && fill.t < tiles) {
+        const uint32_t f = j - 1, sf = f % kQStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + sf * L::kSlot, &full[sf], lane);
+        fill.advance(step, drt, dct, ctiles);
+        ++issued;
+      }
+      return true;
+    };
+    auto load_cols = [&](uint2 (&cv)[16]) {
 #pragma unroll
       for (int k = 0; k < 16; ++k) cv[k] = *reinterpret_cast<const uint2*>(buf + coff + 1024 * k);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    if (warp == 0 && j >= 1 && fill.t < tiles) {
-      // Refill the slot of tile j-1 (every warp released it, usually long
-      // ago) with tile j-1+kQStages.
-      const uint32_t f = j - 1, sf = f % kQStages;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, p.wait_ns, kWeight ? 0x211u : 0x111u);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      quant_fill<kGlu>(&tmx, xrow, C, fill.rt, fill.ct, smem + sf * L::kSlot, &full[sf], lane);
-      fill.advance(step, drt, dct, ctiles);
-      ++issued;
+    };
+    if constexpr (!kCols) {
+      if (!release()) break;
     }
 
     if constexpr (kScale == kScaleMx32) {
@@ -372,6 +397,9 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
         }
       }
       if constexpr (kCols) {
+        uint2 cv[16];
+        load_cols(cv);
+        if (!release()) break;
         uint32_t c01 = 0u, c23 = 0u;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -380,98 +408,110 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
         }
         c01 = bf16x2_maxabs(c01, __shfl_xor_sync(0xffffffffu, c01, 16));
         c23 = bf16x2_maxabs(c23, __shfl_xor_sync(0xffffffffu, c23, 16));
-        const GroupScale gs0 = make_group_scale_mx(fabsf(bf16lo(c01))), gs1 = make_group_scale_mx(fabsf(bf16hi(c01)));
-        const GroupScale gs2 = make_group_scale_mx(fabsf(bf16lo(c23))), gs3 = make_group_scale_mx(fabsf(bf16hi(c23)));
+        const GroupScale gs[4] = {make_group_scale_mx(fabsf(bf16lo(c01))), make_group_scale_mx(fabsf(bf16hi(c01))),
+                                  make_group_scale_mx(fabsf(bf16lo(c23))), make_group_scale_mx(fabsf(bf16hi(c23)))};
         if (g < 4)  // the 4 scales of this lane's columns for 32-group g of the tile's rows
           *reinterpret_cast<float4*>(p.sT + (static_cast<int64_t>(cur.rt) * 4 + g) * p.C + c0 + 16 * warp + 4 * cq) =
-              make_float4(gs0.s, gs1.s, gs2.s, gs3.s);
-        uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
-        *reinterpret_cast<uint4*>(qcol) = quant_col16<0, 0, true, kScaleMx32>(cv, gs0);
-        *reinterpret_cast<uint4*>(qcol + p.R) = quant_col16<0, 1, true, kScaleMx32>(cv, gs1);
-        *reinterpret_cast<uint4*>(qcol + 2 * p.R) = quant_col16<1, 0, true, kScaleMx32>(cv, gs2);
-        *reinterpret_cast<uint4*>(qcol + 3 * p.R) = quant_col16<1, 1, true, kScaleMx32>(cv, gs3);
+              make_float4(gs[0].s, gs[1].s, gs[2].s, gs[3].s);
+        quant_col_codes<true, kScaleMx32>(cv, gs, p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg, p.R);
       }
       continue;
     }
 
-    // amaxes (packed bf16, NaN ignored)
-    float row_m = 0.0f;
-    uint32_t m01 = 0u, m23 = 0u;
-    if constexpr (kRows) {
-      uint32_t m2 = 0u;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        m2 = bf16x2_maxabs(bf16x2_maxabs(m2, bf16x2_maxabs(rv[k].x, rv[k].y)), bf16x2_maxabs(rv[k].z, rv[k].w));
-      row_m = bf16x2_absmax(m2);
-      row_m = fmaxf(row_m, __shfl_xor_sync(0xffffffffu, row_m, 1));
-    }
-    if constexpr (kCols) {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        m01 = bf16x2_maxabs(m01, cv[k].x);
-        m23 = bf16x2_maxabs(m23, cv[k].y);
-      }
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        m01 = bf16x2_maxabs(m01, __shfl_xor_sync(0xffffffffu, m01, o));
-        m23 = bf16x2_maxabs(m23, __shfl_xor_sync(0xffffffffu, m23, o));
-      }
-    }
-
-    GroupScale grow, gc[4];  // this lane's row group; its 4 columns' groups
-    bool all_exact;
-    if constexpr (kWeight) {
-      // one block: every warp's maxima meet in shared memory.  Slot j%2 is
-      // reused two tiles later, when every warp has read it (a warp arrives
-      // for tile j+1 only after reading slot j%2).
-      float m = kRows ? row_m : fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23));
+    // Block maximum of a weight tile: every warp's maximum meets in shared
+    // memory.  Slot j%2 is reused two tiles later, when every warp has read
+    // it (a warp arrives for tile j+1 only after reading slot j%2).
+    auto block_max = [&](float m, bool& ok) -> float {
       m = warp_max(m);
       float* rbuf = red + (j & 1u) * kQComputeWarps;
       if (lane == 0) {
         rbuf[warp] = m;
         mbar_arrive(&redbar[j & 1u]);
       }
-      if (!mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, p.wait_ns, 0x221u)) break;
+      ok = mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, p.wait_ns, 0x221u);
       float bm = rbuf[0];
 #pragma unroll
       for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
-      grow = make_scale<kScale>(bm);
+      return bm;
+    };
+
+    GroupScale grow;  // the row group's scale (weights: the block's)
+    if constexpr (kRows) {
+      uint32_t m2 = 0u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) gc[k] = grow;
-      all_exact = grow.exact;  // uniform over the block
-      if (threadIdx.x == 0) p.s[cur.rt * static_cast<int64_t>(ctiles) + cur.ct] = grow.s;
-    } else {
-      bool ok = true;
-      if constexpr (kRows) {
+      for (int k = 0; k < 8; ++k)
+        m2 = bf16x2_maxabs(bf16x2_maxabs(m2, bf16x2_maxabs(rv[k].x, rv[k].y)), bf16x2_maxabs(rv[k].z, rv[k].w));
+      float row_m = bf16x2_absmax(m2);
+      row_m = fmaxf(row_m, __shfl_xor_sync(0xffffffffu, row_m, 1));
+      bool fast;
+      if constexpr (kWeight) {
+        bool ok;
+        grow = make_scale<kScale>(block_max(row_m, ok));
+        if (!ok) break;
+        if (threadIdx.x == 0) p.s[cur.rt * static_cast<int64_t>(ctiles) + cur.ct] = grow.s;
+        fast = grow.exact;  // uniform over the block
+      } else {
         grow = make_scale<kScale>(row_m);
-        ok = grow.exact;
         if (hh == 0) p.s[static_cast<int64_t>(cur.ct) * p.R + r0 + wrow] = grow.s;
+        fast = kScale == kScaleMulRecip || __all_sync(0xffffffffu, grow.exact);  // no slow path for the multiplier
       }
-      if constexpr (kCols) {
+      uint8_t* qrow = p.q + (r0 + wrow) * p.C + c0 + 16 * hh;
+      if (fast)
+        quant_row_codes<true, kScale>(rv, grow, qrow);
+      else
+        quant_row_codes<false, kScale>(rv, grow, qrow);
+    }
+
+    if constexpr (kCols) {
+      uint2 cv[16];
+      load_cols(cv);
+      if (!release()) break;
+      uint32_t m01 = 0u, m23 = 0u;
+      if (!(kWeight && kRows)) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          m01 = bf16x2_maxabs(m01, cv[k].x);
+          m23 = bf16x2_maxabs(m23, cv[k].y);
+        }
+      }
+      GroupScale gc[4];  // the groups of this lane's 4 columns
+      bool fast;
+      if constexpr (kWeight) {
+        if constexpr (!kRows) {
+          bool ok;
+          grow = make_scale<kScale>(block_max(fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23)), ok));
+          if (!ok) break;
+          if (threadIdx.x == 0) p.s[cur.rt * static_cast<int64_t>(ctiles) + cur.ct] = grow.s;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gc[k] = grow;
+        fast = grow.exact;
+      } else {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          m01 = bf16x2_maxabs(m01, __shfl_xor_sync(0xffffffffu, m01, o));
+          m23 = bf16x2_maxabs(m23, __shfl_xor_sync(0xffffffffu, m23, o));
+        }
         // lane (cq, g) forms the scale of column 4cq + g%4; lanes cq + 4k
         // hold those of this lane's columns
         const int sel = g & 3;
         const uint32_t mw = sel < 2 ? m01 : m23;
         const GroupScale gcol = make_scale<kScale>(fabsf((sel & 1) ? bf16hi(mw) : bf16lo(mw)));
-        ok = ok && gcol.exact;
         if (g < 4) p.sT[static_cast<int64_t>(cur.rt) * p.C + c0 + 16 * warp + 4 * cq + g] = gcol.s;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           gc[k].s = __shfl_sync(0xffffffffu, gcol.s, cq + 4 * k);
           gc[k].r = __shfl_sync(0xffffffffu, gcol.r, cq + 4 * k);
-          gc[k].exact = true;  // restated from s on the slow path
+          gc[k].exact = scale_fast<kScale>(gc[k].s);
         }
+        fast = kScale == kScaleMulRecip || __all_sync(0xffffffffu, gcol.exact);
       }
-      all_exact = __all_sync(0xffffffffu, ok);
+      uint8_t* qcol = p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg;
+      if (fast)
+        quant_col_codes<true, kScale>(cv, gc, qcol, p.R);
+      else
+        quant_col_codes<false, kScale>(cv, gc, qcol, p.R);
     }
-
-    // codes
-    uint8_t* qrow = kRows ? p.q + (r0 + wrow) * p.C + c0 + 16 * hh : nullptr;
-    uint8_t* qcol = kCols ? p.qT + (c0 + 16 * warp + 4 * cq) * p.R + r0 + 16 * rg : nullptr;
-    if (kScale == kScaleMulRecip || all_exact)  // the multiplier mode has no slow path
-      quant_tile_codes<kMode, true, kScale>(rv, cv, grow, gc, qrow, qcol, p.R);
-    else
-      quant_tile_codes<kMode, false, kScale>(rv, cv, grow, gc, qrow, qcol, p.R);
   }
   // Leave no copy in flight into this CTA's shared memory: after an early
   // exit at local tile j, warp 0 (which issues every copy) waits (bounded)

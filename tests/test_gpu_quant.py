@@ -78,6 +78,26 @@ def test_edge_values(scale_mode):
     check_w(xb, scale_mode)
 
 
+def test_non_finite_inputs():
+    """Infinities and NaNs (amax/448 mode).  A group holding an infinity has
+    s = inf: its finite values code as signed zeros (x / inf) and its
+    infinities as NaN (inf / inf); a NaN codes as NaN (0x7F) in any group,
+    and the amax ignores it.  The codes and scales match the oracle's."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((256, 384)).astype(np.float32)
+    x[0, 0] = np.inf
+    x[0, 1], x[0, 2] = -2.0, -0.0
+    x[1, 5], x[1, 6] = np.nan, -np.nan
+    x[2, 3] = -np.inf
+    x[3, :128] = 0.0
+    x[3, 9] = np.nan                      # a group of zeros and one NaN: s = 1
+    x[130, 200] = np.inf                  # a token group (rows 128..255) with an infinity
+    x[140:150, 300] = np.nan
+    xb = workloads.to_bf16(x)
+    check_act(xb)
+    check_w(xb)
+
+
 @pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
 def test_every_bf16_bit_pattern(scale_mode):
     bits = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)

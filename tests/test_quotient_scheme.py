@@ -22,6 +22,7 @@ against an exact rational search.
 """
 
 import numpy as np
+import pytest
 
 
 def _fma32_exact(a, b, c):
@@ -176,3 +177,88 @@ def test_pow2_exponent_from_bits_is_the_smallest_covering_power():
     for a, kv in zip(amax[::97], k[::97]):  # exact rationals on a stride
         fa = F(float(a))
         assert F(2) ** int(kv) * 448 >= fa > F(2) ** (int(kv) - 1) * 448
+
+
+def test_step_on_negated_x_keeps_every_quotient_and_the_sign_of_zero():
+    """The quantisers run the step on nx = -x with nr = -RN(1/s):
+    y0 = RN(nx nr), e = RN(s y0 + nx), Q = RN(e nr + y0).  Over the same
+    exhaustive binade, both signs of x and both zeros, Q must be the IEEE
+    quotient bit for bit, sign of zero included (-0 / s = -0)."""
+    bf = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    bf = bf[(bf == 0) | (bf >= 2.0 ** -30)]
+    n = 0
+    for mant in range(0, 128, 3):
+        amax = np.float32(1.0 + mant / 128.0)
+        s = amax / np.float32(448.0)
+        nr = -(np.float32(1.0) / s)
+        xp = bf[bf <= amax]
+        x = np.concatenate([xp, -xp])
+        nx = -x
+        y0 = nx * nr
+        e = _fma32_exact(y0, np.full_like(x, s), nx)
+        q = _fma32_exact(e, np.full_like(x, nr), y0)
+        want = x / s
+        assert np.array_equal(q.view(np.uint32), want.view(np.uint32)), mant
+        n += x.size
+    assert n > 300_000
+    # the step on x itself loses the sign of -0 (the reason for the negated form)
+    x0 = np.array([-0.0], np.float32)
+    s = np.float32(1.0) / np.float32(448.0)
+    r = np.float32(1.0) / s
+    y0 = x0 * r
+    q_plain = _fma32_exact(np.full_like(x0, r), _fma32_exact(-np.full_like(x0, s), y0, x0), y0)
+    assert not np.signbit(q_plain[0])
+
+
+def _scaled_quotient(x, s):
+    """The quantisers' path for a group scale off the FMA range: p = 2^100
+    for s < 1, 2^-64 otherwise, 0 for an infinite s (then s p := 1); two
+    correction steps on nxp = -x p with nr = -RN(1 / (s p))."""
+    if np.isinf(s):
+        p, sp = np.float32(0.0), np.float32(1.0)
+    else:
+        p = np.float32(2.0 ** 100) if s < 1 else np.float32(2.0 ** -64)
+        sp = s * p
+    nr = -(np.float32(1.0) / sp)
+    with np.errstate(invalid="ignore", under="ignore", over="ignore"):
+        nxp = (-x) * p
+        y0 = nxp * nr
+        sv, nrv = np.full_like(x, sp), np.full_like(x, nr)
+        y1 = _fma32_exact(_fma32_exact(y0, sv, nxp), nrv, y0)
+        return _fma32_exact(_fma32_exact(y1, sv, nxp), nrv, y1)
+
+
+@pytest.mark.parametrize("amax_bits", [0x00010000, 0x00800000, 0x02800000, 0x08C00000, 0x0F230000,
+                                       0x76000000, 0x76A30000, 0x7A000000, 0x7F7F0000])
+def test_prescaled_path_for_extreme_scales(amax_bits):
+    """Groups with s = RN(amax/448) outside [2^-80, 2^100] (fp32-subnormal
+    scales included): every bf16 x with |x| <= amax, both signs.  The code
+    (E4M3 magnitude and sign) must be that of the IEEE quotient, and so must
+    Q's bits wherever the quotient is a normal fp32."""
+    amax = np.array([amax_bits], np.uint32).view(np.float32)[0]
+    with np.errstate(under="ignore"):
+        s = amax / np.float32(448.0)
+    assert not (2.0 ** -80 <= s <= 2.0 ** 100)
+    bf = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    xp = bf[bf <= amax]
+    x = np.concatenate([xp, -xp])
+    q = _scaled_quotient(x, s)
+    with np.errstate(under="ignore"):
+        want = x / s
+    assert np.array_equal(np.signbit(q), np.signbit(want))
+    assert np.array_equal(_e4m3_index(np.abs(q)), _e4m3_index(np.abs(want)))
+    normal = np.abs(want) >= 2.0 ** -126
+    assert np.array_equal(q[normal].view(np.uint32), want[normal].view(np.uint32))
+    assert normal[x == amax].all()  # amax / s, near 448, is among them
+
+
+def test_prescaled_path_for_an_infinite_scale():
+    """amax = inf (an infinite input): x / inf is a signed zero for finite x
+    and NaN for infinite x; the path with p = 0 gives the same."""
+    x = np.array([0.0, -0.0, 1.0, -3.5, 3e38, -1e-40, np.inf, -np.inf], np.float32)
+    q = _scaled_quotient(x, np.float32(np.inf))
+    with np.errstate(invalid="ignore"):
+        want = x / np.float32(np.inf)
+    fin = np.isfinite(x)
+    assert np.array_equal(q[fin].view(np.uint32), want[fin].view(np.uint32))
+    assert np.all(np.isnan(q[~fin])) and np.all(np.isnan(want[~fin]))
