@@ -11,12 +11,19 @@ c_p = ctypes.c_void_p
 c_sz = ctypes.c_size_t
 c_int = ctypes.c_int
 
+
+class WJob(ctypes.Structure):
+    """bfp8_w_job: one weight of bfp8_quantize_w_128x128_batch."""
+    _fields_ = [("w", c_p), ("n", c_i64), ("k", c_i64), ("q", c_p), ("qT", c_p), ("s", c_p)]
+
+
 # name -> (restype, argtypes), in the order the header declares them
 SIGNATURES = {
     "bfp8_quantize_act_1x128": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p]),
     "bfp8_quantize_w_128x128": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p]),
     "bfp8_quantize_act_1x128_ex": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_int, c_p]),
     "bfp8_quantize_w_128x128_ex": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_int, c_p]),
+    "bfp8_quantize_w_128x128_batch": (c_int, [ctypes.POINTER(WJob), c_int, c_int, c_p]),
     "bfp8_swiglu_quantize_1x128": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p, c_int, c_p]),
     "bfp8_quantize_mx_1x32": (c_int, [c_p, c_i64, c_i64, c_p, c_p, c_p, c_p, c_p]),
     "bfp8_mx_gemm": (c_int, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p, c_p]),

@@ -98,6 +98,22 @@ bfp8_status device_state(DeviceState** out) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxSmem::kAlloc);
 #undef BFP8_SET_QUANT_SMEM_ALL
+#define BFP8_SET_WBATCH_SMEM(MODE, SCALE)                                                                \
+  if (e == cudaSuccess)                                                                                  \
+    e = cudaFuncSetAttribute(quantize_w_batch_kernel<MODE, SCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             kQuantSmemBytes);                                                           \
+  if (e == cudaSuccess)                                                                                  \
+    e = cudaFuncSetAttribute(quantize_w_batch_kernel<MODE, SCALE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+#define BFP8_SET_WBATCH_SMEM_ALL(SCALE)        \
+  BFP8_SET_WBATCH_SMEM(kQRows, SCALE)          \
+  BFP8_SET_WBATCH_SMEM(kQCols, SCALE)          \
+  BFP8_SET_WBATCH_SMEM(kQRows | kQCols, SCALE)
+    BFP8_SET_WBATCH_SMEM_ALL(kScaleAmax448)
+    BFP8_SET_WBATCH_SMEM_ALL(kScalePow2)
+    BFP8_SET_WBATCH_SMEM_ALL(kScaleMulRecip)
+#undef BFP8_SET_WBATCH_SMEM_ALL
+#undef BFP8_SET_WBATCH_SMEM
+    // the SiLU-gated prologue#undef BFP8_SET_QUANT_SMEM_ALL
     // the SiLU-gated prologue: one CTA per SM with two tiles per ring slot
 #define BFP8_SET_GLU_SMEM_ALL(SCALE)                                                      \
   BFP8_SET_QUANT_SMEM_GLU(false, kQRows, SCALE, true, kQuantGluSmemBytes)                 \
@@ -592,6 +608,68 @@ bfp8_status quant_w_impl(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_
   return launch_quant(p, true, scale_mode, stream);
 }
 
+// Launches of the batched weight quantiser, kQBatch jobs at a time; every
+// job is checked before the first launch.
+template <int kScale>
+void launch_quant_w_batch(int mode, const QuantBatchParams& b, unsigned grid, cudaStream_t st) {
+  if (mode == kQRows)
+    quantize_w_batch_kernel<kQRows, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(b);
+  else if (mode == kQCols)
+    quantize_w_batch_kernel<kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(b);
+  else
+    quantize_w_batch_kernel<kQRows | kQCols, kScale><<<grid, kQuantThreads, kQuantSmemBytes, st>>>(b);
+}
+
+bfp8_status quant_w_batch_impl(const bfp8_w_job* jobs, int count, int scale_mode, cudaStream_t stream) {
+  if (!scale_mode_ok(scale_mode) || jobs == nullptr || count < 1) return BFP8_EINVAL;
+  const bool rows = jobs[0].q != nullptr, cols = jobs[0].qT != nullptr;
+  for (int i = 0; i < count; ++i) {
+    const bfp8_w_job& jb = jobs[i];
+    if (!jb.w || !jb.s || (jb.q != nullptr) != rows || (jb.qT != nullptr) != cols || (!rows && !cols))
+      return BFP8_EINVAL;
+    if (!dim_ok(jb.n) || !dim_ok(jb.k) || jb.k > (int64_t(1) << 27)) return BFP8_EINVAL;
+    if (!aligned16(jb.w) || !aligned16(jb.s) || (rows && !aligned16(jb.q)) || (cols && !aligned16(jb.qT)))
+      return BFP8_EALIGN;
+  }
+  DeviceState* dev = nullptr;
+  bfp8_status st = device_state(&dev);
+  if (st != BFP8_OK) return st;
+  const int mode = (rows ? kQRows : 0) | (cols ? kQCols : 0);
+  for (int i0 = 0; i0 < count; i0 += kQBatch) {
+    QuantBatchParams b{};
+    const int n = std::min(kQBatch, count - i0);
+    int64_t tiles = 0;
+    for (int k = 0; k < n; ++k) {
+      const bfp8_w_job& jb = jobs[i0 + k];
+      if ((st = make_quant_tmap(&b.tm[k], jb.w, jb.n, jb.k)) != BFP8_OK) return st;
+      QuantJob& q = b.job[k];
+      q.q = jb.q;
+      q.qT = jb.qT;
+      q.s = jb.s;
+      q.R = jb.n;
+      q.C = jb.k;
+      q.ctiles = static_cast<uint32_t>(jb.k / 128);
+      q.tile0 = static_cast<uint32_t>(tiles);
+      tiles += (jb.n / 128) * (jb.k / 128);
+      if (tiles >= (int64_t(1) << 31)) return BFP8_EINVAL;
+    }
+    b.jobs = static_cast<uint32_t>(n);
+    b.tiles = static_cast<uint32_t>(tiles);
+    b.wait_ns = dev->wait_ns;
+    b.stall = take_stall();
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, int64_t(dev->sms) * 2));
+    if (scale_mode == kScalePow2)
+      launch_quant_w_batch<kScalePow2>(mode, b, grid, stream);
+    else if (scale_mode == kScaleMulRecip)
+      launch_quant_w_batch<kScaleMulRecip>(mode, b, grid, stream);
+    else
+      launch_quant_w_batch<kScaleAmax448>(mode, b, grid, stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if ((st = cuda_status(cudaGetLastError())) != BFP8_OK) return st;
+  }
+  return BFP8_OK;
+}
+
 // Workspace carving for the fused linear calls: consecutive 256-byte aligned
 // regions.
 struct Carver {
@@ -727,6 +805,11 @@ bfp8_status bfp8_quantize_act_1x128_ex(const void* x, int64_t M, int64_t K, uint
 bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K, uint8_t* q, uint8_t* qT, float* s,
                                        bfp8_scale_mode scale_mode, bfp8_stream_t stream) {
   return quant_w_impl(w, N, K, q, qT, s, scale_mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bfp8_status bfp8_quantize_w_128x128_batch(const bfp8_w_job* jobs, int count, bfp8_scale_mode scale_mode,
+                                          bfp8_stream_t stream) {
+  return quant_w_batch_impl(jobs, count, scale_mode, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bfp8_status bfp8_swiglu_quantize_1x128(const void* gu, int64_t M, int64_t F, void* h, uint8_t* q, float* s,

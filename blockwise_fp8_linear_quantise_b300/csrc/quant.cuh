@@ -525,4 +525,188 @@ __global__ void __launch_bounds__(kQuantThreads, kGlu ? 1 : 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Several weights in one launch.  A Transformer layer quantises four weights
+// of 8-50 MB each; one launch per weight leaves a persistent grid mostly in
+// its ramp-up and drain (a 2048 x 2048 weight has 256 tiles for 296 CTAs).
+// This kernel walks the 128 x 128 blocks of up to kQBatch weights as one
+// sequence (job 0's tiles, then job 1's, ...), each fetched through its own
+// tensor map, with the weight path of quantize_tile_kernel: one block scale
+// per tile, rows coded before columns.  Every job writes the same outputs
+// (kMode).
+constexpr int kQBatch = 4;
+
+struct QuantJob {
+  uint8_t* q;      // [R, C] (kQRows)
+  uint8_t* qT;     // [C, R] (kQCols)
+  float* s;        // [R/128, C/128]
+  int64_t R, C;
+  uint32_t ctiles;  // C/128
+  uint32_t tile0;   // first tile of this job in the walk
+};
+
+struct QuantBatchParams {
+  CUtensorMap tm[kQBatch];  // bf16 [R/16, 16 C] views, as make_quant_tmap builds them
+  QuantJob job[kQBatch];
+  uint32_t jobs, tiles;     // jobs in use; tiles of all of them
+  uint64_t wait_ns;
+  uint32_t stall;           // test hook, as QuantParams::stall
+};
+
+// The job, row tile and column tile of walk position t.
+struct BatchTile {
+  uint32_t j, rt, ct;
+};
+__device__ __forceinline__ BatchTile batch_tile(const QuantBatchParams& b, uint32_t t) {
+  uint32_t j = 0;
+#pragma unroll
+  for (int k = 1; k < kQBatch; ++k)
+    if (static_cast<uint32_t>(k) < b.jobs && t >= b.job[k].tile0) j = static_cast<uint32_t>(k);
+  const uint32_t lt = t - b.job[j].tile0;
+  return {j, lt / b.job[j].ctiles, lt % b.job[j].ctiles};
+}
+
+template <int kMode, int kScale>
+__global__ void __launch_bounds__(kQuantThreads, 2) quantize_w_batch_kernel(const __grid_constant__ QuantBatchParams b) {
+  using L = QuantLayout<false>;
+  constexpr bool kRows = (kMode & kQRows) != 0, kCols = (kMode & kQCols) != 0;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + kQStages;
+  uint64_t* redbar = empty + kQStages;  // block amax exchange, by tile parity
+  uint64_t* stall = redbar + 2;         // never completed (test hook b.stall)
+  float* red = reinterpret_cast<float*>(smem + L::kRedOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tiles = b.tiles, step = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kQComputeWarps);
+    }
+    mbar_init(&redbar[0], kQComputeWarps);
+    mbar_init(&redbar[1], kQComputeWarps);
+    mbar_init(stall, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Warp 0 issues the first kQStages tiles, and later (at iteration j) tile
+  // j-1+kQStages into the slot tile j-1 used.
+  uint32_t fill_t = blockIdx.x, issued = 0;
+  auto fill = [&](uint32_t slot) {
+    const BatchTile f = batch_tile(b, fill_t);
+    quant_fill<false>(&b.tm[f.j], static_cast<uint32_t>(b.job[f.j].C), 0u, f.rt, f.ct, smem + slot * L::kSlot,
+                      &full[slot], lane);
+    fill_t += step;
+    ++issued;
+  };
+  const bool stalled = b.stall != 0u && warp == 0 && !mbar_wait(stall, 0, b.wait_ns, 0x240u);
+  if (warp == 0 && !stalled) {
+    while (issued < kQStages && fill_t < tiles) fill(issued);
+  }
+
+  // lane maps as in quantize_tile_kernel
+  const int jj = lane >> 1, hh = lane & 1;
+  const int ra = (jj & 1) | (((jj >> 2) & 1) << 1) | (((jj >> 1) & 1) << 2);
+  const int wrow = 16 * ra + 2 * warp + (jj >> 3);
+  const uint32_t roff = 1024u * (2 * warp + (jj >> 3)) + 128u * ra + ((static_cast<uint32_t>(2 * hh) ^ ra) << 4);
+  const int cq = lane & 3, g = lane >> 2, rg = 2 * (g & 3) + (g >> 2);
+  const uint32_t coff = 16384u * (warp >> 2) + 128u * rg +
+                        ((static_cast<uint32_t>(2 * (warp & 3) + (cq >> 1)) ^ rg) << 4) + 8u * (cq & 1);
+
+  uint32_t j = 0;
+  for (uint32_t t = blockIdx.x; t < tiles; t += step, ++j) {
+    const uint32_t s = j % kQStages, ph = (j / kQStages) & 1u;
+    if (!mbar_wait(&full[s], ph, b.wait_ns, 0x241u)) break;
+    uint8_t* buf = smem + s * L::kSlot;
+    const BatchTile bt = batch_tile(b, t);
+    const QuantJob& job = b.job[bt.j];
+    const int64_t r0 = static_cast<int64_t>(bt.rt) * 128, c0 = static_cast<int64_t>(bt.ct) * 128;
+
+    auto release = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (warp == 0 && j >= 1 && fill_t < tiles) {
+        const uint32_t f = j - 1, sf = f % kQStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[sf], (f / kQStages) & 1u, b.wait_ns, 0x242u);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        fill(sf);
+      }
+      return true;
+    };
+    auto block_max = [&](float m, bool& ok) -> float {
+      m = warp_max(m);
+      float* rbuf = red + (j & 1u) * kQComputeWarps;
+      if (lane == 0) {
+        rbuf[warp] = m;
+        mbar_arrive(&redbar[j & 1u]);
+      }
+      ok = mbar_wait(&redbar[j & 1u], (j >> 1) & 1u, b.wait_ns, 0x243u);
+      float bm = rbuf[0];
+#pragma unroll
+      for (int k = 1; k < kQComputeWarps; ++k) bm = fmaxf(bm, rbuf[k]);
+      return bm;
+    };
+
+    GroupScale gb;  // the block's scale
+    if constexpr (kRows) {
+      uint4 rv[8];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        rv[2 * m] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1))));
+        rv[2 * m + 1] = *reinterpret_cast<const uint4*>(buf + 16384 * (m >> 1) + (roff ^ (64u * (m & 1) + 16u)));
+      }
+      if constexpr (!kCols) {
+        if (!release()) break;
+      }
+      uint32_t m2 = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        m2 = bf16x2_maxabs(bf16x2_maxabs(m2, bf16x2_maxabs(rv[k].x, rv[k].y)), bf16x2_maxabs(rv[k].z, rv[k].w));
+      bool ok;
+      gb = make_scale<kScale>(block_max(bf16x2_absmax(m2), ok));
+      if (!ok) break;
+      if (threadIdx.x == 0) job.s[bt.rt * static_cast<int64_t>(job.ctiles) + bt.ct] = gb.s;
+      uint8_t* qrow = job.q + (r0 + wrow) * job.C + c0 + 16 * hh;
+      if (gb.exact)
+        quant_row_codes<true, kScale>(rv, gb, qrow);
+      else
+        quant_row_codes<false, kScale>(rv, gb, qrow);
+    }
+    if constexpr (kCols) {
+      uint2 cv[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) cv[k] = *reinterpret_cast<const uint2*>(buf + coff + 1024 * k);
+      if (!release()) break;
+      if constexpr (!kRows) {
+        uint32_t m01 = 0u, m23 = 0u;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          m01 = bf16x2_maxabs(m01, cv[k].x);
+          m23 = bf16x2_maxabs(m23, cv[k].y);
+        }
+        bool ok;
+        gb = make_scale<kScale>(block_max(fmaxf(bf16x2_absmax(m01), bf16x2_absmax(m23)), ok));
+        if (!ok) break;
+        if (threadIdx.x == 0) job.s[bt.rt * static_cast<int64_t>(job.ctiles) + bt.ct] = gb.s;
+      }
+      const GroupScale gc[4] = {gb, gb, gb, gb};
+      uint8_t* qcol = job.qT + (c0 + 16 * warp + 4 * cq) * job.R + r0 + 16 * rg;
+      if (gb.exact)
+        quant_col_codes<true, kScale>(cv, gc, qcol, job.R);
+      else
+        quant_col_codes<false, kScale>(cv, gc, qcol, job.R);
+    }
+  }
+  // No copy left in flight into shared memory (see quantize_tile_kernel).
+  if (warp == 0 && lane == 0) {
+    for (uint32_t k = j; k < issued; ++k)
+      mbar_wait(&full[k % kQStages], (k / kQStages) & 1u, kDrainWaitNs, 0x244u);
+  }
+}
+
 }  // namespace bfp8

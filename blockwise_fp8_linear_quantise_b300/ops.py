@@ -142,6 +142,27 @@ def quantize_w_128x128(w, want_q=True, want_qT=True, q=None, qT=None, s=None, st
     return q, qT, s
 
 
+def quantize_w_batch(ws, want_q=True, want_qT=True, outs=None, stream=None, scale_mode="amax448"):
+    """Quantise several bf16 weights (each [N, K]) in 128x128 blocks with one
+    launch per four weights -> [(q, qT, s), ...], each as quantize_w_128x128
+    returns it.  outs: optional [(q, qT, s), ...] to write into."""
+    lib = _lib.load()
+    res = []
+    jobs = (_lib.WJob * len(ws))()
+    for i, w in enumerate(ws):
+        N, K = w.shape
+        _need(w, torch.bfloat16, (N, K), "w")
+        oq, oqT, os_ = outs[i] if outs is not None else (None, None, None)
+        q = _out(oq, torch.uint8, (N, K), w.device, "q") if want_q else None
+        qT = _out(oqT, torch.uint8, (K, N), w.device, "qT") if want_qT else None
+        s = _out(os_, torch.float32, (N // 128, K // 128), w.device, "s")
+        jobs[i] = _lib.WJob(_ptr(w), N, K, _ptr(q), _ptr(qT), _ptr(s))
+        res.append((q, qT, s))
+    _check(lib.bfp8_quantize_w_128x128_batch(jobs, len(ws), _scale_mode(scale_mode), _stream(stream)),
+           "quantize_w_batch")
+    return res
+
+
 def quantize_mx_1x32(x, rows=True, tokens=False, q=None, s=None, qT=None, sT=None, stream=None):
     """MXFP8 1x32 quantisation of bf16 x [M, K] (power-of-two scales per 32 values).
 

@@ -141,6 +141,35 @@ bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K,
                                        bfp8_scale_mode scale_mode, bfp8_stream_t stream);
 
 /*
+ * Several weights quantised by one launch (the rule of
+ * bfp8_quantize_w_128x128_ex applied to each; "Puro-2B ...", section 3.2:
+ * 128x128 weight blocks).  A Transformer layer quantises four weights of
+ * 8-50 MB each, and one launch per weight spends much of its time filling and
+ * draining the GPU; this call walks the blocks of all of them in one launch
+ * (up to four weights per launch, several launches for more) and writes
+ * exactly what count calls of bfp8_quantize_w_128x128_ex would write.
+ *
+ *   jobs   host array of count descriptors, read during the call only; each
+ *          names a weight w bf16 [n, k] and its outputs q [n, k], qT [k, n],
+ *          s [n/128, k/128] (device pointers, 16-byte aligned), with the same
+ *          meaning and the same rules as bfp8_quantize_w_128x128.
+ *   count  number of jobs, >= 1.
+ * Every job must ask for the same outputs: all give q or all leave it NULL,
+ * and the same for qT.  Errors: EINVAL (a bad job, count < 1, mixed
+ * outputs, unknown scale_mode), EALIGN, ECUDA; nothing is launched when a job
+ * is rejected.
+ */
+typedef struct {
+  const void* w;
+  int64_t n, k;
+  uint8_t* q;
+  uint8_t* qT;
+  float* s;
+} bfp8_w_job;
+bfp8_status bfp8_quantize_w_128x128_batch(const bfp8_w_job* jobs, int count, bfp8_scale_mode scale_mode,
+                                          bfp8_stream_t stream);
+
+/*
  * SiLU-gated FFN activation fused into the activation quantiser: the input of
  * the FFN's down projection, h = bf16_rn(SiLU(g) * u) with
  * SiLU(g) = g / (1 + e^-g), is formed from the fused gate+up output and

@@ -118,3 +118,23 @@ def test_workspace_sizes_cover_the_intermediates():
     assert bwd >= 2 * M * N + (N // 128) * M * 4 + (M // 128) * N * 4  # dYq + dYqT + scales
     assert lib.bfp8_linear_fwd_workspace_bytes(M, N, 100) == 0
     assert lib.bfp8_gemm_workspace_bytes(0, 100, 128, 128) == 0
+
+
+def test_weight_batch_rejects_bad_jobs():
+    from blockwise_fp8_linear_quantise_b300._lib import WJob
+    lib = _lib.load()
+    f = lib.bfp8_quantize_w_128x128_batch
+    good = lambda: WJob(FAKE, 256, 128, FAKE, FAKE, FAKE)
+    jobs = (WJob * 3)(good(), good(), good())
+    assert f(None, 1, 0, None) == EINVAL
+    assert f(jobs, 0, 0, None) == EINVAL
+    assert f(jobs, 3, 7, None) == EINVAL                      # unknown scale mode
+    for bad, want in ((WJob(None, 256, 128, FAKE, FAKE, FAKE), EINVAL),   # no weight
+                      (WJob(FAKE, 256, 128, FAKE, FAKE, None), EINVAL),   # no scales
+                      (WJob(FAKE, 256, 128, None, FAKE, FAKE), EINVAL),   # outputs differ from job 0's
+                      (WJob(FAKE, 200, 128, FAKE, FAKE, FAKE), EINVAL),   # not a multiple of 128
+                      (WJob(MIS, 256, 128, FAKE, FAKE, FAKE), EALIGN),
+                      (WJob(FAKE, 256, 128, FAKE, MIS, FAKE), EALIGN)):
+        jobs[2] = bad
+        assert f(jobs, 3, 0, None) == want
+    assert f((WJob * 1)(WJob(FAKE, 256, 128, None, None, FAKE)), 1, 0, None) == EINVAL  # no output at all

@@ -71,6 +71,18 @@ def test_quantisers_stay_inside_their_outputs(M, K):
         assert torch.equal(gw[k].t, w), k
 
 
+def test_weight_batch_stays_inside_its_outputs():
+    shapes = [(384, 640), (128, 128), (1152, 256)]
+    xs = [bf16(sh, sum(sh)) for sh in shapes]
+    gs = [guarded(Wq=((M, K), torch.uint8), WqT=((K, M), torch.uint8), sW=((M // 128, K // 128), torch.float32))
+          for M, K in shapes]
+    ops.quantize_w_batch(xs, outs=[(g["Wq"].t, g["WqT"].t, g["sW"].t) for g in gs])
+    for g, x in zip(gs, xs):
+        check_all(g)
+        for k, w in zip(("Wq", "WqT", "sW"), ops.quantize_w_128x128(x)):
+            assert torch.equal(g[k].t, w), k
+
+
 def test_swiglu_prologue_stays_inside_its_outputs():
     M, F = 384, 256
     gu = bf16((M, 2 * F), 7, 0.5)

@@ -343,3 +343,46 @@ def test_stack_weights_all_layers():
                 assert_scales_equal(s.cpu().numpy(), os_, f"sW {tag} layer {layer}")
     finally:
         parallel.shutdown()
+
+
+@pytest.mark.parametrize("scale_mode", ["amax448", "pow2", "mul_recip"])
+@pytest.mark.parametrize("outputs", ["both", "q", "qT"])
+def test_weight_batch_matches_the_oracle(scale_mode, outputs):
+    """Six weights of different shapes (two launches: four, then two) quantised
+    by bfp8_quantize_w_128x128_batch: every job's codes and scales equal the
+    oracle's and those of its own single call, bit for bit."""
+    shapes = [(512, 256), (256, 256), (1536, 256), (256, 768), (128, 128), (384, 640)]
+    rng = np.random.default_rng(31)
+    ws = [workloads.to_bf16((rng.standard_normal(sh) * np.exp2(rng.integers(-8, 8))).astype(np.float32))
+          for sh in shapes]
+    want_q, want_qT = outputs in ("both", "q"), outputs in ("both", "qT")
+    got = ops.quantize_w_batch([w.to(dev()) for w in ws], want_q=want_q, want_qT=want_qT, scale_mode=scale_mode)
+    assert ops.sync_status() == 0
+    for w, (q, qT, s) in zip(ws, got):
+        oq, oqT, os_ = quant.quantize_w_128x128(np32(w), scale_mode=scale_mode)
+        assert_scales_equal(s.cpu().numpy(), os_, "sW")
+        if want_q:
+            assert_codes_equal(u8(q), oq, "Wq")
+        if want_qT:
+            assert_codes_equal(u8(qT), oqT, "WqT")
+        sq, sqT, ss = ops.quantize_w_128x128(w.to(dev()), want_q=want_q, want_qT=want_qT, scale_mode=scale_mode)
+        assert torch.equal(ss, s) and (not want_q or torch.equal(sq, q)) and (not want_qT or torch.equal(sqT, qT))
+
+
+def test_weight_batch_on_one_stack_layer():
+    """The four weights of one stack28 layer (QKV, O, gate+up, down), as the
+    step quantises them: one launch, bit-exact against the oracle."""
+    wl = workloads.make("stack28")
+    tags = []
+    for s in wl.linears:
+        if workloads.layer_of(s) == 3 and s.w_tag not in tags:
+            tags.append(s.w_tag)
+    ws = [workloads.tensor(wl, t, 3) for t in tags]
+    assert len(ws) == 4
+    got = ops.quantize_w_batch([w.to(dev()) for w in ws])
+    assert ops.sync_status() == 0
+    for w, (q, qT, s) in zip(ws, got):
+        oq, oqT, os_ = quant.quantize_w_128x128(np32(w))
+        assert_codes_equal(u8(q), oq, "Wq")
+        assert_codes_equal(u8(qT), oqT, "WqT")
+        assert_scales_equal(s.cpu().numpy(), os_, "sW")

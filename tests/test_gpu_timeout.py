@@ -93,6 +93,19 @@ def test_gemm_timeout_then_within_tolerance(layout, kind):
     assert rel_fro(np32(C), want) <= REL_FRO_TOL
 
 
+def test_weight_batch_timeout_then_exact():
+    ws = [operands(256, 384, 5), operands(128, 256, 6)]
+    wg = [w.to("cuda") for w in ws]
+    assert stalled(lambda: ops.quantize_w_batch(wg)) == ETIMEOUT
+    got = ops.quantize_w_batch(wg)
+    assert ops.sync_status() == 0
+    for w, (q, qT, s) in zip(ws, got):
+        oq, oqT, os_ = quant.quantize_w_128x128(np32(w))
+        assert_codes_equal(u8(q), oq, "Wq")
+        assert_codes_equal(u8(qT), oqT, "WqT")
+        assert_scales_equal(s.cpu().numpy(), os_, "sW")
+
+
 def test_stall_hook_affects_one_launch_only():
     x = operands(128, 128, 5).to("cuda")
     assert stalled(lambda: (ops.quantize_act_1x128(x), ops.quantize_act_1x128(x))) == ETIMEOUT
