@@ -133,6 +133,9 @@ def parse_args(argv=None):
     ap.add_argument("--oracle-plan", action="store_true",
                     help="time the CPU oracle on every configuration in full (stack28: layer 0 in full, 1/16 of the "
                          "output tiles of layers 1-27, extrapolated) against the GPU path, checking parity")
+    ap.add_argument("--per-kernel", action="store_true",
+                    help="time each ABI call of one stack layer alone: 10 warm-up calls, then the median of 50, "
+                         "with L2 flushed (a 256 MB write) before every timed call")
     ap.add_argument("--probe-mx", action="store_true",
                     help="compare the MXFP8 1x32 recipe with the blockwise one on the mlp_down layer: accuracy of "
                          "every GEMM against the unquantised product, and time of quantisers and GEMMs")
@@ -994,6 +997,66 @@ def oracle_plan(args):
     return 0
 
 
+def per_kernel_protocol(args):
+    """Each ABI call of one stack28 layer (the batched weight quantiser, then
+    per linear the activation quantiser and FPROP; backward: the output
+    gradient quantiser, DGRAD and WGRAD) timed alone: 10 warm-up calls, then
+    50 timed calls, each preceded by a 256 MB write that evicts L2, with CUDA
+    events on the launching stream around the call only.  Prints one JSON line
+    with the median per call and its rate against the burst peaks (the kernels
+    run alone, unthrottled) and, for the GEMMs, the rate scaled to the
+    sustained peak's clock as well."""
+    import torch
+    from blockwise_fp8_linear_quantise_b300 import build as bld, ops, workloads
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", 0)
+    bld.build()
+    wl = workloads.make("stack28")
+    specs = linear_list(wl, 1)
+    runner = StackRunner(wl, specs, dev, args.scale_mode, False, False)
+    runner.step()
+    torch.cuda.synchronize()
+    if ops.sync_status() != 0:
+        raise SystemExit("device status not ok")
+    peaks, basis = load_peaks()
+    fp8_burst = peaks["bf16_tflops"] * FP8_PER_BF16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(gpu_uuid(dev))
+    clocks.start()
+    rows = []
+    for kind, work, fn, cargs in runner.calls:
+        for _ in range(10):
+            if fn(*cargs, stream.cuda_stream) != 0:
+                raise SystemExit(f"{kind}: call failed")
+        times = []
+        for i in range(50):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(*cargs, stream.cuda_stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) * 1e-3)
+        t = statistics.median(times)
+        gemm = kind in ("fprop", "dgrad", "wgrad")
+        rate = work / t / (1e12 if gemm else 1e9)
+        peak = fp8_burst if gemm else peaks["hbm_gbs"]
+        rows.append({"call": kind, "work": work, "median_us": round(t * 1e6, 2),
+                     ("TFLOP/s" if gemm else "GB/s"): round(rate, 1), "frac_of_burst": round(rate / peak, 4)})
+    clk = clocks.stop()
+    if ops.sync_status() != 0:
+        raise SystemExit("device status not ok after the protocol")
+    shapes = [[s.M, s.N, s.K] for s in specs]
+    print(json.dumps({"per_kernel_protocol": "stack28 layer 0", "shapes_MNK": shapes, "scale_mode": args.scale_mode,
+                      "protocol": "10 warm-up calls, median of 50, 256 MB L2 flush before each timed call",
+                      "peaks": {"fp8_burst_TFLOP/s": round(fp8_burst, 1), "hbm_GB/s": peaks["hbm_gbs"],
+                                "basis": f"{basis}: 2 x bf16 burst; HBM copy"},
+                      "clocks": clk, "calls": rows}), flush=True)
+    return 0
+
+
 def mx_probe(args):
     """The MXFP8 1x32 recipe against the blockwise 1x128 / 128x128 recipe on
     the mlp_down layer (X [8192, 6144], W [2048, 6144], dY [8192, 2048]):
@@ -1107,6 +1170,8 @@ def main(argv=None):
         return swiglu_probe(args)
     if args.probe_mx:
         return mx_probe(args)
+    if args.per_kernel:
+        return per_kernel_protocol(args)
     if args.oracle_plan:
         return oracle_plan(args)
     if args.impl == "reference":
