@@ -54,8 +54,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch,
-# averaged over the launches of one stack layer (the same 24 launches as
-# every layer of the step), from an ncu capture of
+# averaged over the launches of one stack layer (the same launches as every
+# layer of the step: 24, or 21 with the batched weight quantiser), from an
+# ncu capture of
 #   python bench.py --layers 1 --steps 1 --warmup 0 --no-e2e --no-cpu-baseline
 # Valid only for the kernel code whose hash (comments ignored) is the key;
 # once the kernels change the bench line reports null until a new capture is
@@ -63,6 +64,8 @@ FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : BF16 tensor rate on B300
 TRAFFIC = {
     "ad55d462807144a1": {"gemm": 232.3e6, "quant": 155.8e6},
     "1508b235cee025dc": {"gemm": 231.9e6, "quant": 155.5e6},
+    # a layer's four weights in one batched launch: 21 launches per layer
+    "e056ae426709bae9": {"gemm": 232.5e6, "quant": 213.2e6},
 }
 
 
