@@ -156,8 +156,9 @@ bfp8_status bfp8_quantize_w_128x128_ex(const void* w, int64_t N, int64_t K,
  *   count  number of jobs, >= 1.
  * Every job must ask for the same outputs: all give q or all leave it NULL,
  * and the same for qT.  Errors: EINVAL (a bad job, count < 1, mixed
- * outputs, unknown scale_mode), EALIGN, ECUDA; nothing is launched when a job
- * is rejected.
+ * outputs, unknown scale_mode) and EALIGN are found before anything is
+ * launched; ECUDA (a tensor-map encode or launch failure) can come after the
+ * launches of earlier groups of four jobs, whose outputs are then written.
  */
 typedef struct {
   const void* w;
