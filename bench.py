@@ -549,10 +549,12 @@ class StackRunner:
 
     # ------------------------------------------------------------ e2e arm
     def e2e_setup(self):
-        """Pinned host copies of every input; pinned host buffers for the
-        weight gradients."""
+        """Pinned host copies of every input, a second device copy of the
+        inputs (so that a step's inputs can be uploaded while the previous step
+        computes), pinned host buffers for the weight gradients."""
         torch = self.torch
         self.h_inputs = {k: v.cpu().pin_memory() for k, v in self.inputs.items()}
+        self.d_sets = [self.inputs, {k: torch.empty_like(v) for k, v in self.inputs.items()}]
         self.h_dW = [None if d is None else torch.empty(d.shape, dtype=d.dtype, pin_memory=True) for d in self.dW]
         # forward-only linears read back their outputs instead
         self.h_out = [None if s.backward else torch.empty((s.M, s.N), dtype=torch.bfloat16, pin_memory=True)
@@ -560,19 +562,31 @@ class StackRunner:
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in self.h_inputs.values())
         self.d2h_bytes = (sum(d.numel() * d.element_size() for d in self.dW if d is not None) +
                           sum(h.numel() * h.element_size() for h in self.h_out if h is not None))
-
-    def e2e_step(self):
-        """Host inputs -> device, fused public calls, weight gradients -> host.
-
-        Copies run on their own streams so that PCIe traffic overlaps the
-        kernels: each linear's inputs are uploaded ahead of it (upload stream),
-        and each weight gradient is read back as soon as its WGRAD is done
-        (download stream), both directions at once.  A step starts only after
-        the previous one finished reading its inputs, and ends once its last
-        read-back is complete.
-        """
+        # upload order of one step: the forward's inputs in layer order, then
+        # the output gradients in the order the backward uses them
         from blockwise_fp8_linear_quantise_b300 import workloads
+        order = []
+        for s in self.specs:
+            for key in ((s.x_tag, None), (s.w_tag, workloads.layer_of(s))):
+                if key not in order:
+                    order.append(key)
+        for s in reversed(self.specs):
+            if s.backward and (s.dy_tag, None) not in order:
+                order.append((s.dy_tag, None))
+        self.upload_order = order
+
+    def e2e_run(self, steps):
+        """`steps` end-to-end steps on the current stream: host inputs ->
+        device, the fused public calls, weight gradients -> host.
+
+        Copies run on their own streams and overlap the kernels.  Step i's
+        inputs go to device copy i % 2: step 0's are uploaded first, and step
+        i + 1's are uploaded while step i computes, once step i - 1 has
+        finished with that copy.  Each weight gradient is read back as soon as
+        its WGRAD is done.  Every step's uploads and read-backs happen inside
+        the call, which returns once the last read-back is complete."""
         torch, ops = self.torch, self.ops
+        from blockwise_fp8_linear_quantise_b300 import workloads
         ms = torch.cuda.current_stream()
         if not hasattr(self, "_up"):
             self._up, self._down = torch.cuda.Stream(), torch.cuda.Stream()
@@ -580,50 +594,70 @@ class StackRunner:
         start = torch.cuda.Event()
         start.record(ms)
         up.wait_event(start)
-        uploaded = {}
+        down.wait_event(start)
+        set_free = [start, start]  # compute finished with device copy k
+        dw_read = {}               # weight gradient j read back (previous step)
 
-        def need(key):
-            if key not in uploaded:
-                with torch.cuda.stream(up):
-                    self.inputs[key].copy_(self.h_inputs[key], non_blocking=True)
+        def upload(k):
+            """Uploads one step's inputs into device copy k; returns their events."""
+            evs = {}
+            up.wait_event(set_free[k])
+            with torch.cuda.stream(up):
+                for key in self.upload_order:
+                    self.d_sets[k][key].copy_(self.h_inputs[key], non_blocking=True)
                     ev = torch.cuda.Event()
                     ev.record(up)
-                uploaded[key] = ev
-            return uploaded[key]
+                    evs[key] = ev
+            return evs
 
-        for i, s in enumerate(self.specs):
-            keys = [(s.x_tag, None), (s.w_tag, workloads.layer_of(s))]
-            evs = [need(k) for k in keys]
-            for ev in evs:
-                ms.wait_event(ev)
-            Y = self.scratch[(s.M, s.N, s.K)]["Y"]
-            ops.linear_fwd(self.inputs[keys[0]], self.inputs[keys[1]], Y=Y, saved=self.saved[i], workspace=self.ws,
-                           scale_mode=self.scale_mode)
-            if not s.backward:
+        pending = upload(0)
+        for i in range(steps):
+            k = i % 2
+            inputs, evs = self.d_sets[k], pending
+            if i + 1 < steps:
+                pending = upload(1 - k)
+            for j, s in enumerate(self.specs):
+                keys = [(s.x_tag, None), (s.w_tag, workloads.layer_of(s))]
+                for key in keys:
+                    ms.wait_event(evs[key])
+                Y = self.scratch[(s.M, s.N, s.K)]["Y"]
+                ops.linear_fwd(inputs[keys[0]], inputs[keys[1]], Y=Y, saved=self.saved[j], workspace=self.ws,
+                               scale_mode=self.scale_mode)
+                if not s.backward:
+                    done = torch.cuda.Event()
+                    done.record(ms)
+                    down.wait_event(done)
+                    with torch.cuda.stream(down):
+                        self.h_out[j].copy_(Y, non_blocking=True)
+                    # the next step's forward writes Y again only after this read
+                    rd = torch.cuda.Event()
+                    rd.record(down)
+                    ms.wait_event(rd)
+            for j in reversed(range(len(self.specs))):
+                s = self.specs[j]
+                if not s.backward:
+                    continue
+                ms.wait_event(evs[(s.dy_tag, None)])
+                if j in dw_read:
+                    ms.wait_event(dw_read[j])  # the previous step's read-back of dW[j] is done
+                dX = self.scratch[(s.M, s.N, s.K)]["dX"]
+                ops.linear_bwd(inputs[(s.dy_tag, None)], self.saved[j], dX=dX, dW=self.dW[j], workspace=self.ws,
+                               scale_mode=self.scale_mode)
                 done = torch.cuda.Event()
                 done.record(ms)
                 down.wait_event(done)
                 with torch.cuda.stream(down):
-                    self.h_out[i].copy_(Y, non_blocking=True)
-        for i, s in enumerate(self.specs):  # output gradients queue behind the forward inputs
-            if s.backward:
-                need((s.dy_tag, None))
-        for i in reversed(range(len(self.specs))):
-            s = self.specs[i]
-            if not s.backward:
-                continue
-            ms.wait_event(need((s.dy_tag, None)))
-            dX = self.scratch[(s.M, s.N, s.K)]["dX"]
-            ops.linear_bwd(self.inputs[(s.dy_tag, None)], self.saved[i], dX=dX, dW=self.dW[i], workspace=self.ws,
-                           scale_mode=self.scale_mode)
-            done = torch.cuda.Event()
-            done.record(ms)
-            down.wait_event(done)
-            with torch.cuda.stream(down):
-                self.h_dW[i].copy_(self.dW[i], non_blocking=True)
+                    self.h_dW[j].copy_(self.dW[j], non_blocking=True)
+                    rd = torch.cuda.Event()
+                    rd.record(down)
+                dw_read[j] = rd
+            fin = torch.cuda.Event()
+            fin.record(ms)
+            set_free[k] = fin
         end = torch.cuda.Event()
         end.record(down)
         ms.wait_event(end)
+        ms.wait_event(set_free[(steps - 1) % 2])
 
 
 def interval_stats(marks):
@@ -775,8 +809,7 @@ def gpu_arm(args):
                "skipped": "measured for the default step only (fused linear_fwd / linear_bwd with bf16 dW)"}
     elif not args.no_e2e:
         runner.e2e_setup()
-        for _ in range(max(1, min(args.warmup, 2))):
-            runner.e2e_step()
+        runner.e2e_run(max(1, min(args.warmup, 2)))
         torch.cuda.synchronize()
         barrier(group)
         torch.cuda.synchronize()
@@ -784,8 +817,7 @@ def gpu_arm(args):
         b = torch.cuda.Event(enable_timing=True)
         a.record()
         e2e_steps = max(1, min(args.steps, 5))
-        for _ in range(e2e_steps):
-            runner.e2e_step()
+        runner.e2e_run(e2e_steps)
         b.record()
         torch.cuda.synchronize()
         barrier(group)
@@ -795,8 +827,9 @@ def gpu_arm(args):
         eflops = sum_over_ranks(flops_step * e2e_steps, group)
         e2e = {"value": eflops / (ems * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": runner.h2d_bytes,
                "d2h_bytes_per_step": runner.d2h_bytes, "ms_per_step": ems / e2e_steps, "steps": e2e_steps,
-               "calls": "linear_fwd / linear_bwd (fused public calls); every input uploaded from pinned host memory "
-                        "and every weight gradient read back, on copy streams overlapping the kernels"}
+               "calls": "linear_fwd / linear_bwd (fused public calls); every step's inputs uploaded from pinned host "
+                        "memory and every weight gradient read back, on copy streams overlapping the kernels (the "
+                        "next step's inputs go up into a second device copy while a step computes)"}
 
     # CPU oracle on a bounded sample (rank 0, single GPU only)
     cpu = None
